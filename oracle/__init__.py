@@ -1,0 +1,162 @@
+"""CPU oracle for MoE dispatch + combine (test infrastructure only).
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library
+and its binding) never imports, links or executes anything in here.
+
+The arithmetic lives in ``moe_oracle.cc`` (plain single-threaded C++,
+written from the definition of the method; the file header cites the passages
+of "Efficient and portable mixture-of-experts communication" and "Enabling
+trillion-parameter models on AWS EFA" it follows).  This module only compiles
+it with the host compiler and marshals numpy arrays through ctypes.
+
+Parity pins: every function here is pinned by the CPU tests
+(``tests/test_oracle_*.py``) against a library stable sort, brute-force
+enumeration, closed-form special cases and an exact rational FMA chain; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.cc")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+OK, EINVAL, EROUTE, EBOUND = 0, 1, 3, 5
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with g++ (no fast-math, no FMA contraction, no
+    -march so that x86 and Arm hosts give identical results)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-o", tmp, _SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+        lib.oracle_dispatch.argtypes = [i32, i32, i32, i32, i32, p, p, p, i64, p, p, p, p, p, p]
+        lib.oracle_dispatch.restype = ctypes.c_int
+        lib.oracle_combine.argtypes = [i32, i32, i32, p, i64, p, p, p]
+        lib.oracle_combine.restype = ctypes.c_int
+        lib.oracle_combine_f64.argtypes = [i32, i32, i32, p, i64, p, p, p, p, p]
+        lib.oracle_combine_f64.restype = ctypes.c_int
+        lib.oracle_float_to_bf16.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_fmaf.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float]
+        lib.oracle_fmaf.restype = ctypes.c_float
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what} failed with oracle status {code}")
+        self.code = code
+
+
+@dataclass
+class Dispatch:
+    expert_x: np.ndarray        # uint16 [rows, H]
+    expert_counts: np.ndarray   # int32 [E]
+    expert_offsets: np.ndarray  # int32 [E+1]
+    src_offsets: np.ndarray     # int32 [E, N]
+    rank_offsets: np.ndarray    # int32 [N+1]
+    slot_row: np.ndarray        # int32 [T, K]
+    row_src: np.ndarray         # int32 [T*K]
+
+
+def dispatch(x: np.ndarray, topk_idx: np.ndarray, E: int, N: int,
+             expert_x_rows: Optional[int] = None) -> Dispatch:
+    """Expert-grouped, stably ordered copy of the token rows plus the routing
+    metadata (see ``oracle_dispatch`` in moe_oracle.cc)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, H = x.shape
+    K = idx.shape[1] if idx.ndim == 2 else 0
+    if idx.shape[0] != T:
+        raise ValueError("x and topk_idx disagree on T")
+    rows = T * K
+    cap = rows if expert_x_rows is None else int(expert_x_rows)
+    ex = np.zeros((max(cap, 0), H), dtype=np.uint16)
+    out = Dispatch(ex, np.zeros(E, np.int32), np.zeros(E + 1, np.int32),
+                   np.zeros((E, N), np.int32), np.zeros(N + 1, np.int32),
+                   np.zeros((T, K), np.int32), np.zeros(rows, np.int32))
+    rc = lib.oracle_dispatch(T, H, K, E, N, _ptr(x), _ptr(idx), _ptr(ex), cap,
+                             _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                             _ptr(out.src_offsets), _ptr(out.rank_offsets),
+                             _ptr(out.slot_row), _ptr(out.row_src))
+    if rc != OK:
+        raise OracleError(rc, "oracle_dispatch")
+    return out
+
+
+def combine(y: np.ndarray, topk_w: np.ndarray, slot_row: np.ndarray) -> np.ndarray:
+    """bf16 out[T, H]: float32 FMA chain over k = 0..K-1 from +0.0, one
+    round-to-nearest-even to bf16."""
+    lib = _load()
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    sr = np.ascontiguousarray(slot_row, dtype=np.int32)
+    T, K = w.shape
+    H = y.shape[1]
+    out = np.zeros((T, H), dtype=np.uint16)
+    rc = lib.oracle_combine(T, H, K, _ptr(y), y.shape[0], _ptr(w), _ptr(sr), _ptr(out))
+    if rc != OK:
+        raise OracleError(rc, "oracle_combine")
+    return out
+
+
+def combine_f64(y: np.ndarray, topk_w: np.ndarray, slot_row: np.ndarray):
+    """(bf16 out, float64 exact-ish sum, float64 sum of |w*y|) of the same
+    weighted sum evaluated in double precision."""
+    lib = _load()
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    sr = np.ascontiguousarray(slot_row, dtype=np.int32)
+    T, K = w.shape
+    H = y.shape[1]
+    out = np.zeros((T, H), dtype=np.uint16)
+    exact = np.zeros((T, H), dtype=np.float64)
+    mag = np.zeros((T, H), dtype=np.float64)
+    rc = lib.oracle_combine_f64(T, H, K, _ptr(y), y.shape[0], _ptr(w), _ptr(sr), _ptr(out),
+                                _ptr(exact), _ptr(mag))
+    if rc != OK:
+        raise OracleError(rc, "oracle_combine_f64")
+    return out, exact, mag
+
+
+def float_to_bf16(f: float) -> int:
+    return int(_load().oracle_float_to_bf16(f))
+
+
+def double_to_bf16(v: float) -> int:
+    return int(_load().oracle_double_to_bf16(v))
+
+
+def fmaf(a: float, b: float, c: float) -> float:
+    return float(_load().oracle_fmaf(a, b, c))

@@ -1,0 +1,273 @@
+// MoE dispatch + combine: the plain CPU oracle.
+//
+// TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+// load this file; only the tests, the smoke check and the benchmark's CPU
+// baseline leg do.  It shares no code, header or constant with the CUDA
+// library: it is written from the definition of the method, single-threaded,
+// with no blocking, fusion or reordering, so that it can be checked by eye.
+//
+// Sources (titles of the pages, with the section used):
+//  * "Efficient and portable mixture-of-experts communication" (pplx-kernels):
+//    - Introduction: the router keeps the top-K experts per token and the
+//      layer output is the router-weighted sum of the experts' outputs.
+//    - Portable kernels: per-rank buffers of fixed capacity, reused by every
+//      layer, with addresses that follow from offsets alone.
+//    - Dispatch: the receiver hands an expert-grouped tensor to the grouped
+//      GEMM and keeps, per row, where the token came from (source rank,
+//      expert, token index) so that combine can send it back.
+//    - Combine: the receiving side computes the weighted sum of all expert
+//      contributions of a token, reading the routing table for which buffer to
+//      read and which weight to apply.
+//  * "Enabling trillion-parameter models on AWS EFA":
+//    - Send and receive buffers: with N ranks of T tokens routed to R of E
+//      experts, one rank receives at most N*T*max(R, E/N) tokens; the bound is
+//      only reached when writes are placed contiguously, which needs the full
+//      routing information (per-expert counts exchanged first, then offsets).
+//    - Dispatch and combine: tokens per expert are counted, a cumulative sum
+//      of the counts gives the offsets of contiguous per-peer buffers, then
+//      tokens are packed at those offsets; combine accumulates only on the
+//      receiving side.
+//
+// Readings where the pages are silent (each one is listed in the design notes):
+//  * expert e lives on logical rank floor(e / (E/N)) (contiguous blocks);
+//  * inside one expert, rows are ordered by global token index t, which is the
+//    same as (source rank, token within rank) because rank s owns tokens
+//    [s*T/N, (s+1)*T/N);
+//  * out-of-range or repeated expert indices within one token are errors;
+//  * router weights are float32; the combine accumulates in float32 with one
+//    fused multiply-add per expert in top-k order starting from +0.0, and
+//    rounds once to bf16 (round to nearest, ties to even); the weighted sum is
+//    not renormalised by the sum of weights.
+//  * A second combine evaluates the same sum in double precision and rounds it
+//    once to bf16: the plain mathematical definition, for error bounds.
+//
+// All bf16 values are raw 16-bit patterns.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+namespace {
+
+enum {
+  ORACLE_OK = 0,
+  ORACLE_EINVAL = 1,  // bad sizes / pointers
+  ORACLE_EROUTE = 3,  // an expert index out of range or repeated in a token
+  ORACLE_EBOUND = 5,  // a rank would receive more rows than the printed bound
+};
+
+float bf16_to_float(uint16_t b) {
+  uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+// IEEE round-to-nearest-even of a finite float to bf16: keep the upper 16
+// bits, rounding on the lower 16 (add 0x7fff plus the lowest kept bit, then
+// truncate).  NaN keeps a quiet-NaN payload.
+uint16_t float_to_bf16_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0)
+    return static_cast<uint16_t>((u >> 16) | 0x0040u);
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// Round a finite double to the nearest bf16 (ties to even) in one step:
+// bf16 keeps 8 significant bits; below the smallest normal (2^-126) the
+// quantum is fixed at 2^-133.
+uint16_t double_to_bf16_rne(double v) {
+  if (v == 0.0) return std::signbit(v) ? 0x8000u : 0x0000u;
+  int e;
+  std::frexp(v, &e);  // |v| = m * 2^e, m in [0.5, 1)
+  int q = e - 8;      // quantum exponent for 8 significant bits
+  if (q < -133) q = -133;
+  double scaled = std::ldexp(v, -q);
+  double r = std::nearbyint(scaled);  // default rounding mode: ties to even
+  double back = std::ldexp(r, q);
+  float f = static_cast<float>(back);  // exact: back has <= 8 significant bits
+  if (std::isinf(f) || std::fabs(back) > 3.3895313892515355e38) {
+    return std::signbit(v) ? 0xff80u : 0x7f80u;
+  }
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+int check_sizes(int32_t T, int32_t H, int32_t K, int32_t E, int32_t N) {
+  if (T < 0 || H < 1 || K < 1 || E < 1 || N < 1) return ORACLE_EINVAL;
+  if (T % N != 0 || E % N != 0 || K > E) return ORACLE_EINVAL;
+  return ORACLE_OK;
+}
+
+// Every expert index is in [0, E) and no token names an expert twice
+// (top-k yields K distinct experts).
+int check_routes(int32_t T, int32_t K, int32_t E, const int32_t* idx) {
+  for (int64_t t = 0; t < T; ++t) {
+    for (int32_t k = 0; k < K; ++k) {
+      int32_t e = idx[t * K + k];
+      if (e < 0 || e >= E) return ORACLE_EROUTE;
+      for (int32_t j = 0; j < k; ++j)
+        if (idx[t * K + j] == e) return ORACLE_EROUTE;
+    }
+  }
+  return ORACLE_OK;
+}
+
+struct Triple {
+  int32_t e;
+  int32_t t;
+  int32_t k;
+};
+
+}  // namespace
+
+extern "C" {
+
+// Dispatch of one layer.
+//   x          bf16 [T, H]   token rows (rank s owns rows [s*T/N, (s+1)*T/N))
+//   topk_idx   int32 [T, K]  experts chosen for each token
+//   expert_x   bf16 [expert_x_rows, H], expert_x_rows >= T*K; rows [0, T*K)
+//              are written in the expert-grouped order, the rest untouched
+//   expert_counts   int32 [E]     rows per expert
+//   expert_offsets  int32 [E+1]   first row of each expert; last = T*K
+//   src_offsets     int32 [E*N]   first row of (expert e, source rank s) at e*N+s
+//   rank_offsets    int32 [N+1]   first row of the experts of rank r; last = T*K
+//   slot_row        int32 [T*K]   row that (t, k) was written to
+//   row_src         int32 [T*K]   for each row, t*K + k of its (token, slot)
+// Returns 0, ORACLE_EINVAL, ORACLE_EROUTE or ORACLE_EBOUND; on error nothing
+// is written.
+int oracle_dispatch(int32_t T, int32_t H, int32_t K, int32_t E, int32_t N,
+                    const uint16_t* x, const int32_t* topk_idx,
+                    uint16_t* expert_x, int64_t expert_x_rows,
+                    int32_t* expert_counts, int32_t* expert_offsets,
+                    int32_t* src_offsets, int32_t* rank_offsets,
+                    int32_t* slot_row, int32_t* row_src) {
+  int rc = check_sizes(T, H, K, E, N);
+  if (rc) return rc;
+  const int64_t rows = static_cast<int64_t>(T) * K;
+  if (expert_x_rows < rows) return ORACLE_EINVAL;
+  if (T > 0 && (!x || !topk_idx || !expert_x)) return ORACLE_EINVAL;
+  rc = check_routes(T, K, E, topk_idx);
+  if (rc) return rc;
+
+  const int32_t Tr = T / N;  // tokens per logical rank
+  const int32_t L = E / N;   // experts per logical rank
+
+  // Counts per expert, and per (source rank, expert).
+  std::vector<int64_t> cnt(E, 0);
+  std::vector<int64_t> src_cnt(static_cast<size_t>(N) * E, 0);
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t s = t / Tr;
+    for (int32_t k = 0; k < K; ++k) {
+      int32_t e = topk_idx[t * K + k];
+      cnt[e] += 1;
+      src_cnt[s * E + e] += 1;
+    }
+  }
+
+  // Exclusive prefix sum of the counts: first row of each expert.
+  std::vector<int64_t> off(E + 1, 0);
+  for (int32_t e = 0; e < E; ++e) off[e + 1] = off[e] + cnt[e];
+
+  // Receive bound per rank: N * (T/N) * max(K, E/N) rows.
+  const int64_t bound = static_cast<int64_t>(N) * Tr * std::max(K, L);
+  for (int32_t r = 0; r < N; ++r) {
+    int64_t recv = off[(r + 1) * L] - off[r * L];
+    if (recv > bound) return ORACLE_EBOUND;
+  }
+
+  // Stable placement: list every (expert, token, slot) in token-major order,
+  // then stable-sort by expert.  Row i of the sorted list is row i of the
+  // grouped buffer.
+  std::vector<Triple> trip;
+  trip.reserve(static_cast<size_t>(rows));
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t k = 0; k < K; ++k) trip.push_back({topk_idx[static_cast<int64_t>(t) * K + k], t, k});
+  std::stable_sort(trip.begin(), trip.end(),
+                   [](const Triple& a, const Triple& b) { return a.e < b.e; });
+
+  for (int64_t i = 0; i < rows; ++i) {
+    const Triple& p = trip[i];
+    int64_t pair = static_cast<int64_t>(p.t) * K + p.k;
+    slot_row[pair] = static_cast<int32_t>(i);
+    row_src[i] = static_cast<int32_t>(pair);
+    std::memcpy(expert_x + i * H, x + static_cast<int64_t>(p.t) * H, sizeof(uint16_t) * H);
+  }
+
+  for (int32_t e = 0; e < E; ++e) expert_counts[e] = static_cast<int32_t>(cnt[e]);
+  for (int32_t e = 0; e <= E; ++e) expert_offsets[e] = static_cast<int32_t>(off[e]);
+  for (int32_t e = 0; e < E; ++e) {
+    int64_t run = off[e];
+    for (int32_t s = 0; s < N; ++s) {
+      src_offsets[static_cast<int64_t>(e) * N + s] = static_cast<int32_t>(run);
+      run += src_cnt[static_cast<int64_t>(s) * E + e];
+    }
+  }
+  for (int32_t r = 0; r <= N; ++r) rank_offsets[r] = static_cast<int32_t>(off[r * L]);
+  return ORACLE_OK;
+}
+
+// Combine of one layer, float32 in top-k order:
+//   out[t, h] = bf16_rne( fma(w[t,K-1], y[slot_row[t,K-1], h], ... fma(w[t,0], y[slot_row[t,0], h], +0.0f)) )
+//   y         bf16 [y_rows, H]  expert outputs in the grouped row layout
+//   topk_w    float32 [T, K]
+//   slot_row  int32 [T*K]       from dispatch
+//   out       bf16 [T, H]
+int oracle_combine(int32_t T, int32_t H, int32_t K, const uint16_t* y, int64_t y_rows,
+                   const float* topk_w, const int32_t* slot_row, uint16_t* out) {
+  if (T < 0 || H < 1 || K < 1) return ORACLE_EINVAL;
+  for (int64_t p = 0; p < static_cast<int64_t>(T) * K; ++p)
+    if (slot_row[p] < 0 || slot_row[p] >= y_rows) return ORACLE_EINVAL;
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t h = 0; h < H; ++h) {
+      float acc = 0.0f;
+      for (int32_t k = 0; k < K; ++k) {
+        int64_t row = slot_row[t * K + k];
+        acc = std::fmaf(topk_w[t * K + k], bf16_to_float(y[row * H + h]), acc);
+      }
+      out[t * H + h] = float_to_bf16_rne(acc);
+    }
+  }
+  return ORACLE_OK;
+}
+
+// The same weighted sum evaluated in double precision (each product of a
+// float32 weight and a bf16 value is exact in double), rounded once to bf16.
+// Also returns, per output element, sum_k |w * y| in abs_sum (may be NULL),
+// which scales the float32 accumulation error bound.
+int oracle_combine_f64(int32_t T, int32_t H, int32_t K, const uint16_t* y, int64_t y_rows,
+                       const float* topk_w, const int32_t* slot_row, uint16_t* out,
+                       double* exact, double* abs_sum) {
+  if (T < 0 || H < 1 || K < 1) return ORACLE_EINVAL;
+  for (int64_t p = 0; p < static_cast<int64_t>(T) * K; ++p)
+    if (slot_row[p] < 0 || slot_row[p] >= y_rows) return ORACLE_EINVAL;
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t h = 0; h < H; ++h) {
+      double acc = 0.0, mag = 0.0;
+      for (int32_t k = 0; k < K; ++k) {
+        int64_t row = slot_row[t * K + k];
+        double term = static_cast<double>(topk_w[t * K + k]) *
+                      static_cast<double>(bf16_to_float(y[row * H + h]));
+        acc += term;
+        mag += std::fabs(term);
+      }
+      out[t * H + h] = double_to_bf16_rne(acc);
+      if (exact) exact[t * H + h] = acc;
+      if (abs_sum) abs_sum[t * H + h] = mag;
+    }
+  }
+  return ORACLE_OK;
+}
+
+// Element-wise helpers exposed for the pins.
+uint16_t oracle_float_to_bf16(float f) { return float_to_bf16_rne(f); }
+uint16_t oracle_double_to_bf16(double v) { return double_to_bf16_rne(v); }
+float oracle_fmaf(float a, float b, float c) { return std::fmaf(a, b, c); }
+
+}  // extern "C"
