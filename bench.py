@@ -1,0 +1,413 @@
+"""Benchmark: one MoE dispatch + combine layer per step on one GB300.
+
+A step is the whole hot path on one batch: moe_dispatch_send (route_count +
+dispatch_pack) -> moe_dispatch_recv -> moe_combine_send -> moe_combine_recv
+(combine), on the DeepSeek-R1-decode-shaped workload by default
+(T = 32 logical ranks x 128 tokens, H = 7168, E = 256, K = 8).  Inputs are
+synthetic, seeded, resident in HBM; the synthetic expert outputs are made
+before timing (no expert GEMM).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on this host's cores
+
+Under torchrun (N > 1) every rank runs an independent replica on its own
+GPU: there is no cross-GPU exchange on this path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine µs/layer and achieved HBM GB/s vs GB300 peak, 1 GPU"
+UNIT = "us/layer"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="deepseek")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--buffer-sets", type=int, default=2)
+    return ap.parse_args()
+
+
+def algorithmic_bytes(w):
+    """Bytes a layer must move at minimum (see the design notes):
+    dispatch reads x and writes T*K rows; combine reads T*K rows and writes T
+    rows; plus the routing metadata."""
+    T, H, K, E, N = w.T, w.H, w.K, w.E, w.N
+    row = H * 2
+    pairs = T * K
+    dispatch = T * row + pairs * row
+    dispatch_meta = 2 * pairs * 4 + 2 * pairs * 4 + pairs * 4 + (3 * E + E * N + N + 2) * 4
+    combine = pairs * row + T * row
+    combine_meta = pairs * 4 + pairs * 4
+    return {"dispatch": dispatch + dispatch_meta, "combine": combine + combine_meta,
+            "total": dispatch + dispatch_meta + combine + combine_meta}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def committed_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or
+    None when the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    entry = rec.get(workload, {}).get(kernel)
+    if not entry:
+        return None
+    src = os.path.join(ROOT, "combine_route_count_gb300", "csrc", entry["source"])
+    try:
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return entry["dram_bytes_per_launch"] if sha == entry["source_sha"] else None
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.index = index
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((parts[0], float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [r[1] for r in rows]
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    """The CPU oracle, as it stands, on this host: each step is one oracle
+    layer (dispatch + combine) over a bounded sample of the workload (the
+    tokens of the first N/8 logical ranks, all experts), scaled to a full
+    layer by the token ratio."""
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from combine_route_count_gb300 import inputs as gen
+    w = gen.BY_NAME[args.workload]
+    oracle.build()
+    li = gen.make_inputs(w)
+    n_s = max(1, w.N // 8)
+    Ts = n_s * w.tokens_per_rank
+    xs, idx_s, w_s = li.x[:Ts], li.topk_idx[:Ts], li.topk_w[:Ts]
+    ys = li.y[:Ts * w.K]
+    for _ in range(args.warmup):
+        d = oracle.dispatch(xs, idx_s, w.E, n_s)
+        oracle.combine(ys, w_s, d.slot_row)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        d = oracle.dispatch(xs, idx_s, w.E, n_s)
+        oracle.combine(ys, w_s, d.slot_row)
+        times.append(time.perf_counter() - t0)
+    scale = w.T / Ts
+    us = statistics.mean(times) * 1e6 * scale
+    sample = f"tokens of the first {n_s} of {w.N} logical ranks ({Ts} of {w.T} tokens) per step, x{scale:g} to a layer"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "higher_is_better": False,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def cpu_baseline(w, li, budget_s=10.0, max_reps=20):
+    """The oracle timed on one host core over the full layer, repeated."""
+    import oracle
+    oracle.build()
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while len(times) < max_reps and (not times or time.perf_counter() < t_end):
+        t0 = time.perf_counter()
+        d = oracle.dispatch(li.x, li.topk_idx, w.E, w.N)
+        oracle.combine(li.y, li.topk_w, d.slot_row)
+        times.append(time.perf_counter() - t0)
+    us = statistics.mean(times) * 1e6
+    return {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"full {w.name} layer (dispatch + combine) x{len(times)}, single-threaded"}
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    from combine_route_count_gb300 import build as build_mod
+    from combine_route_count_gb300 import inputs as gen
+    from combine_route_count_gb300 import moe
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    build_mod.build()
+    moe.load_library()
+
+    w = gen.BY_NAME[args.workload]
+    li = gen.make_inputs(w)
+    T, H, K, E, N = w.T, w.H, w.K, w.E, w.N
+    rows = T * K
+    stream = torch.cuda.Stream(device=dev)
+
+    # Rotating buffer sets: consecutive steps touch different memory, and each
+    # layer's working set (x, y, expert_x, out: ~1 GB at DeepSeek size) is far
+    # larger than the 129 MB L2, so no step starts with its inputs in L2.
+    sets = []
+    with torch.cuda.stream(stream):
+        x0 = torch.from_numpy(li.x.view(np.int16)).to(dev)
+        idx0 = torch.from_numpy(li.topk_idx).to(dev)
+        w0 = torch.from_numpy(li.topk_w).to(dev)
+        y0 = torch.from_numpy(li.y.view(np.int16)).to(dev)
+        for _ in range(args.buffer_sets):
+            sets.append(dict(x=x0.clone(), idx=idx0.clone(), w=w0.clone(), y=y0.clone(),
+                             expert_x=torch.empty((rows, H), dtype=torch.int16, device=dev),
+                             out=torch.empty((T, H), dtype=torch.int16, device=dev)))
+        del x0, idx0, w0, y0
+    torch.cuda.synchronize(dev)
+    layer = moe.MoELayer(T, H, K, E, N, device=dev)
+
+    def step(s):
+        layer.dispatch_send(s["x"], s["idx"], s["expert_x"], stream)
+        layer.dispatch_recv(stream)
+        layer.combine_send(s["y"], stream)
+        layer.combine_recv(s["w"], s["out"], stream)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for i in range(args.warmup):
+        step(sets[i % len(sets)])
+    if layer.get_error(stream) != moe.MOE_OK:
+        raise RuntimeError("device reported an error during warm-up")
+
+    clocks = ClockSampler(torch.cuda.current_device() if ws == 1 else local).start()
+    time.sleep(0.2)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        s = sets[i % len(sets)]
+        ev[i][0].record(stream)
+        layer.dispatch_send(s["x"], s["idx"], s["expert_x"], stream)
+        ev[i][1].record(stream)
+        layer.dispatch_recv(stream)
+        layer.combine_send(s["y"], stream)
+        layer.combine_recv(s["w"], s["out"], stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall1 = time.time()
+    clk = clocks.stop(t_wall0, t_wall1)
+    status = layer.get_error(stream)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device reported status {status} in the timed region")
+
+    layer_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    disp_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    comb_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    ms_step = total_ms / args.steps
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    us_layer = ms_step * 1e3
+
+    ab = algorithmic_bytes(w)
+    peak, peak_kind = measured_peaks()
+    disp_us = statistics.mean(disp_ms) * 1e3
+    comb_us = statistics.mean(comb_ms) * 1e3
+    kernels = {
+        "dispatch_send": {"us": round(disp_us, 2), "bytes": ab["dispatch"],
+                          "gbs": round(ab["dispatch"] / disp_us / 1e3, 1),
+                          "kernels": ["route_count", "dispatch_pack"]},
+        "combine_recv": {"us": round(comb_us, 2), "bytes": ab["combine"],
+                         "gbs": round(ab["combine"] / comb_us / 1e3, 1), "kernels": ["combine"]},
+    }
+    if comb_us >= disp_us:
+        dom, dom_us, dom_bytes, dom_kernel, dom_src = "combine", comb_us, ab["combine"], "combine", "combine.cu"
+    else:
+        dom, dom_us, dom_bytes, dom_kernel, dom_src = ("route_count+dispatch_pack", disp_us, ab["dispatch"],
+                                                       "dispatch_pack", "dispatch_pack.cu")
+    achieved = dom_bytes / dom_us / 1e3
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": committed_traffic(dom_kernel, w.name),
+                "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, li, layer, stream, dev)
+
+    cpu = None
+    if not args.no_cpu and rank == 0 and ws == 1:
+        cpu = cpu_baseline(w, li)
+    elif not args.no_cpu and rank == 0:
+        cpu = cpu_baseline(w, li)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(us_layer, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
+                       "parallelism": "replicas" if ws > 1 else "single",
+                       "l2": f"inputs > L2: {ab['total'] / 1e6:.0f} MB moved per layer, "
+                             f"{args.buffer_sets} rotating buffer sets",
+                       "pack": "bulk (TMA) 4 stages, PDL"},
+            "achieved_gbs": round(ab["total"] / us_layer / 1e3, 1),
+            "hbm_frac": round(ab["total"] / us_layer / 1e3 / peak, 4),
+            "algorithmic_bytes_per_layer": ab["total"],
+            "layer_us_median": round(statistics.median(layer_ms) * 1e3, 2),
+            "kernels": kernels,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clk,
+            "gpu_launches": 3 * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, li, layer, stream, dev):
+    """The same layer through the public API with HOST buffers: every step
+    copies x, topk_idx, topk_w and the expert outputs y from pinned host
+    memory, runs the four calls, and copies out back to pinned host memory."""
+    import numpy as np
+    import torch
+    T, H, K = w.T, w.H, w.K
+    hx = torch.from_numpy(li.x.view(np.int16)).pin_memory()
+    hidx = torch.from_numpy(li.topk_idx).pin_memory()
+    hw = torch.from_numpy(li.topk_w).pin_memory()
+    hy = torch.from_numpy(li.y.view(np.int16)).pin_memory()
+    hout = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    dx = torch.empty_like(hx, device=dev)
+    didx = torch.empty_like(hidx, device=dev)
+    dw = torch.empty_like(hw, device=dev)
+    dy = torch.empty_like(hy, device=dev)
+    dex = torch.empty((T * K, H), dtype=torch.int16, device=dev)
+    dout = torch.empty((T, H), dtype=torch.int16, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hidx, hw, hy))
+    d2h = hout.numel() * hout.element_size()
+
+    def step():
+        with torch.cuda.stream(stream):
+            dx.copy_(hx, non_blocking=True)
+            didx.copy_(hidx, non_blocking=True)
+            dw.copy_(hw, non_blocking=True)
+            dy.copy_(hy, non_blocking=True)
+            layer.dispatch_send(dx, didx, dex, stream)
+            layer.dispatch_recv(stream)
+            layer.combine_send(dy, stream)
+            layer.combine_recv(dw, dout, stream)
+            hout.copy_(dout, non_blocking=True)
+
+    steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) / steps * 1e3
+    return {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

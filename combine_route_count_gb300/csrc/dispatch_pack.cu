@@ -1,0 +1,194 @@
+// dispatch_pack: expert_x[slot_row[t, k]] = x[t] for every token t and slot k.
+//
+// "Enabling trillion-parameter models on AWS EFA" (Dispatch and combine):
+// once the offsets are known, every token is packed into the send buffer at
+// its offset.  "Efficient and portable mixture-of-experts communication"
+// (Portable kernels; Dispatch): dispatch-send is parallelised over the tokens
+// of a rank, and the receiver's layout is the grouped-GEMM input.  On one GPU
+// the send buffer and the receive layout are the same memory, so one copy
+// places each row directly ("Further improvements": shared buffers remove
+// copies).
+//
+// Each token row is read from HBM once and written K times.  Work is split
+// into units (token t, piece j of the row); CTA b takes units b, b+G, b+2G...
+//
+// Bulk variant (default): one warp per CTA drives the TMA engine.  Lane 0
+// loads a piece into a shared-memory stage with cp.async.bulk (completion on
+// an mbarrier), then lanes 0..K-1 each store the stage to one destination row
+// with cp.async.bulk (bulk async-groups).  A stage is refilled once every
+// lane's store group has finished reading it.  The first loads are issued
+// before griddepcontrol.wait: token rows do not depend on route_count, so
+// under programmatic dependent launch they overlap it.
+//
+// Vector variant: each warp copies a unit with 16-byte loads and K 16-byte
+// stores per chunk, no shared memory.
+
+#include <cuda_runtime.h>
+
+#include "moe_kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxStages = 8;
+constexpr int kBarBytes = 128;  // mbarrier block at the front of shared memory
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase.  False if it did not complete in time.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const unsigned long long start = globaltimer();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (globaltimer() - start > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void report(int32_t* error_word, int status) {
+  atomicCAS(error_word, MOE_OK, status);
+}
+
+__global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stages) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* stage_buf = smem + kBarBytes;
+  const int lane = threadIdx.x;
+  const int64_t units = static_cast<int64_t>(p.T) * p.pieces;
+  const int64_t first = blockIdx.x;
+  const int64_t step = gridDim.x;
+  const int64_t mine = units > first ? (units - first + step - 1) / step : 0;
+
+  if (lane == 0) {
+    for (int s = 0; s < stages; ++s) ptx::mbar_init(&bars[s], 1);
+    ptx::mbar_fence_init();
+  }
+  __syncwarp();
+
+  auto piece_bytes = [&](int j) -> uint32_t {
+    const int64_t left = p.row_bytes - static_cast<int64_t>(j) * p.piece_bytes;
+    return static_cast<uint32_t>(left < p.piece_bytes ? left : p.piece_bytes);
+  };
+  auto issue_load = [&](int64_t i) {
+    const int64_t u = first + i * step;
+    const int64_t t = u / p.pieces;
+    const int j = static_cast<int>(u - t * p.pieces);
+    const uint32_t bytes = piece_bytes(j);
+    const int s = static_cast<int>(i % stages);
+    ptx::mbar_arrive_expect_tx(&bars[s], bytes);
+    ptx::bulk_g2s(stage_buf + static_cast<size_t>(s) * p.piece_bytes,
+                  p.x + t * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes, bytes, &bars[s]);
+  };
+
+  // Token rows are ready before this grid starts: prefetch while the routing
+  // kernel is still running.
+  const int64_t prologue = mine < stages ? mine : stages;
+  if (lane == 0)
+    for (int64_t i = 0; i < prologue; ++i) issue_load(i);
+
+  ptx::wait_prerequisites();  // slot_row is written by route_count
+
+  int64_t i = 0;
+  bool ok = true;
+  for (; i < mine; ++i) {
+    const int64_t u = first + i * step;
+    const int64_t t = u / p.pieces;
+    const int j = static_cast<int>(u - t * p.pieces);
+    const int s = static_cast<int>(i % stages);
+    const int row = lane < p.K ? p.slot_row[t * p.K + lane] : -1;  // coherent load: written by the previous grid
+    // Every lane waits; the outcome is made warp-uniform so that no lane is
+    // left behind at a later __syncwarp.
+    const bool arrived = wait_phase(&bars[s], static_cast<uint32_t>((i / stages) & 1));
+    if (!__all_sync(0xffffffffu, arrived)) {
+      ok = false;
+      break;
+    }
+    if (row >= 0) {
+      ptx::bulk_s2g(p.expert_x + static_cast<int64_t>(row) * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes,
+                    stage_buf + static_cast<size_t>(s) * p.piece_bytes, piece_bytes(j));
+    }
+    ptx::bulk_commit();
+    // Refill the stage of unit i-1 once every lane's stores of unit i-1
+    // have read it (the stores of unit i stay in flight).
+    if (i >= 1 && i - 1 + stages < mine) {
+      ptx::bulk_wait_read<1>();
+      __syncwarp();
+      if (lane == 0) issue_load(i - 1 + stages);
+    }
+  }
+  if (!ok) {
+    if (lane == 0) {
+      report(p.error_word, MOE_ETIMEDOUT);
+      // Loads issued so far: the prologue's [0, prologue) and, from the
+      // refills of iterations 1..i-1, units up to i-2+stages.  Wait (bounded)
+      // for those not yet consumed before the CTA exits.
+      int64_t last = prologue - 1;
+      if (i >= 2 && i - 2 + stages > last) last = i - 2 + stages;
+      if (last > mine - 1) last = mine - 1;
+      for (int64_t q = i; q <= last; ++q) wait_phase(&bars[q % stages], static_cast<uint32_t>((q / stages) & 1));
+    }
+    __syncwarp();
+  }
+  ptx::bulk_wait<0>();  // stores complete before shared memory goes away
+}
+
+__global__ void __launch_bounds__(256) dispatch_pack_vector(PackParams p) {
+  ptx::wait_prerequisites();
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t units = static_cast<int64_t>(p.T) * p.pieces;
+  for (int64_t u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += warps) {
+    const int64_t t = u / p.pieces;
+    const int j = static_cast<int>(u - t * p.pieces);
+    const int my_row = lane < p.K ? p.slot_row[t * p.K + lane] : -1;
+    const int64_t off = static_cast<int64_t>(j) * p.piece_bytes;
+    const int64_t left = p.row_bytes - off;
+    const int chunks = static_cast<int>((left < p.piece_bytes ? left : p.piece_bytes) >> 4);
+    const uint8_t* src = p.x + t * p.row_bytes + off;
+    for (int c0 = 0; c0 < chunks; c0 += 4 * 32) {
+      uint4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int c = c0 + q * 32 + lane;
+        if (c < chunks) v[q] = ptx::ld_stream_v4(src + static_cast<int64_t>(c) * 16);
+      }
+      for (int k = 0; k < p.K; ++k) {
+        const int row = __shfl_sync(0xffffffffu, my_row, k);
+        if (row < 0) continue;
+        uint8_t* dst = p.expert_x + static_cast<int64_t>(row) * p.row_bytes + off;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int c = c0 + q * 32 + lane;
+          if (c < chunks) ptx::st_v4(dst + static_cast<int64_t>(c) * 16, v[q]);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+size_t pack_bulk_smem_bytes(int stages, int piece_bytes) {
+  return kBarBytes + static_cast<size_t>(stages) * piece_bytes;
+}
+
+cudaError_t prepare_pack(int max_smem_bytes) {
+  return cudaFuncSetAttribute(dispatch_pack_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_bytes);
+}
+
+cudaError_t launch_dispatch_pack(const PackParams& p, const PackLaunch& l, cudaStream_t stream) {
+  if (l.variant == kPackVector) {
+    return launch_kernel(dispatch_pack_vector, dim3(l.grid), dim3(256), 0, stream, l.pdl, p);
+  }
+  const int stages = l.stages < 2 ? 2 : (l.stages > kMaxStages ? kMaxStages : l.stages);
+  return launch_kernel(dispatch_pack_bulk, dim3(l.grid), dim3(32), pack_bulk_smem_bytes(stages, p.piece_bytes),
+                       stream, l.pdl, p, stages);
+}
+
+}  // namespace moe

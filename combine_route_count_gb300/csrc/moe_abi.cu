@@ -1,0 +1,371 @@
+// The C ABI of libmoe.so (declared in include/moe.h): argument checks, the
+// workspace layout, the send/recv phase machine and the kernel launches.
+//
+// The split send/recv pairs follow "Efficient and portable
+// mixture-of-experts communication" (Portable kernels: each kernel pair owns
+// fixed-capacity buffers that every layer reuses; Dispatch; Combine) and
+// "Enabling trillion-parameter models on AWS EFA" (Dispatch and combine).
+// On one GPU nothing travels between ranks, so the receive halves are
+// ordering points: dispatch_recv hands out the layout, combine_send registers
+// the expert outputs, and the gather + weighted sum runs in combine_recv.
+
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "moe.h"
+#include "moe_kernels.cuh"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+enum Phase { kIdle = 0, kDispatched = 1, kReceived = 2, kCombineSent = 3 };
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct WorkspaceLayout {
+  size_t error_word, expert_counts, expert_offsets, src_offsets, rank_offsets, slot_row, row_src, total;
+};
+
+WorkspaceLayout layout_of(const moe_config& c) {
+  WorkspaceLayout l;
+  const size_t pairs = static_cast<size_t>(c.num_tokens) * c.top_k;
+  size_t o = 0;
+  l.error_word = o;
+  o += align_up(sizeof(int32_t));
+  l.expert_counts = o;
+  o += align_up(sizeof(int32_t) * c.num_experts);
+  l.expert_offsets = o;
+  o += align_up(sizeof(int32_t) * (c.num_experts + 1));
+  l.src_offsets = o;
+  o += align_up(sizeof(int32_t) * static_cast<size_t>(c.num_experts) * c.num_ranks);
+  l.rank_offsets = o;
+  o += align_up(sizeof(int32_t) * (c.num_ranks + 1));
+  l.slot_row = o;
+  o += align_up(sizeof(int32_t) * pairs);
+  l.row_src = o;
+  o += align_up(sizeof(int32_t) * pairs);
+  l.total = o;
+  return l;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+struct moe_ctx {
+  moe_config cfg;
+  uint8_t* ws;
+  size_t ws_bytes;
+  int device;
+  int num_sms;
+  int max_smem_optin;
+  int phase;
+  const void* expert_y;
+  int64_t expert_y_rows;
+  int32_t* error_word;
+  int32_t* expert_counts;
+  int32_t* expert_offsets;
+  int32_t* src_offsets;
+  int32_t* rank_offsets;
+  int32_t* slot_row;
+  int32_t* row_src;
+  // launch options (MOE_OPT_* in moe.h)
+  int pack_variant;
+  int pack_stages;
+  int pack_piece_bytes;  // 0 = automatic
+  int pack_ctas_per_sm;  // 0 = as many as fit
+  int pdl;
+};
+
+MOE_API int moe_validate_config(const moe_config* c) {
+  if (!c) return MOE_EINVAL;
+  if (c->num_tokens < 0 || c->num_ranks < 1 || c->num_experts < 1 || c->top_k < 1) return MOE_EINVAL;
+  if (c->hidden < 8 || c->hidden % 8 != 0) return MOE_EINVAL;
+  if (c->top_k > MOE_MAX_TOP_K || c->top_k > c->num_experts) return MOE_EINVAL;
+  if (c->num_experts > MOE_MAX_EXPERTS) return MOE_EINVAL;
+  if (c->num_tokens % c->num_ranks != 0 || c->num_experts % c->num_ranks != 0) return MOE_EINVAL;
+  if (static_cast<int64_t>(c->num_tokens) * c->top_k > INT32_MAX) return MOE_EINVAL;
+  if (static_cast<int64_t>(c->num_experts) * c->num_ranks > INT32_MAX / 4) return MOE_EINVAL;
+  return MOE_OK;
+}
+
+MOE_API int moe_workspace_bytes(const moe_config* cfg, size_t* bytes) {
+  if (!bytes) return MOE_EINVAL;
+  const int rc = moe_validate_config(cfg);
+  if (rc) return rc;
+  *bytes = layout_of(*cfg).total;
+  return MOE_OK;
+}
+
+MOE_API int moe_recv_bound_rows(const moe_config* cfg, int64_t* rows) {
+  if (!rows) return MOE_EINVAL;
+  const int rc = moe_validate_config(cfg);
+  if (rc) return rc;
+  const int64_t Tr = cfg->num_tokens / cfg->num_ranks;
+  const int64_t L = cfg->num_experts / cfg->num_ranks;
+  *rows = static_cast<int64_t>(cfg->num_ranks) * Tr * (cfg->top_k > L ? cfg->top_k : L);
+  return MOE_OK;
+}
+
+MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t workspace_bytes, moe_ctx** out) {
+  if (!out) return MOE_EINVAL;
+  *out = nullptr;
+  int rc = moe_validate_config(cfg);
+  if (rc) return rc;
+  const WorkspaceLayout l = layout_of(*cfg);
+  if (!workspace || workspace_bytes < l.total || !aligned(workspace, kAlign)) return MOE_EINVAL;
+
+  int dev = 0, sms = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ECUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ECUDA;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return MOE_ECUDA;
+  if (moe::route_count_smem_bytes(cfg->num_experts) > static_cast<size_t>(optin)) return MOE_EINVAL;
+  if (moe::prepare_pack(optin) != cudaSuccess) return MOE_ECUDA;
+
+  moe_ctx* c = new (std::nothrow) moe_ctx;
+  if (!c) return MOE_EINVAL;
+  std::memset(c, 0, sizeof *c);
+  c->cfg = *cfg;
+  c->ws = static_cast<uint8_t*>(workspace);
+  c->ws_bytes = workspace_bytes;
+  c->device = dev;
+  c->num_sms = sms;
+  c->max_smem_optin = optin;
+  c->phase = kIdle;
+  c->error_word = reinterpret_cast<int32_t*>(c->ws + l.error_word);
+  c->expert_counts = reinterpret_cast<int32_t*>(c->ws + l.expert_counts);
+  c->expert_offsets = reinterpret_cast<int32_t*>(c->ws + l.expert_offsets);
+  c->src_offsets = reinterpret_cast<int32_t*>(c->ws + l.src_offsets);
+  c->rank_offsets = reinterpret_cast<int32_t*>(c->ws + l.rank_offsets);
+  c->slot_row = reinterpret_cast<int32_t*>(c->ws + l.slot_row);
+  c->row_src = reinterpret_cast<int32_t*>(c->ws + l.row_src);
+  c->pack_variant = moe::kPackBulk;
+  c->pack_stages = 4;
+  c->pack_piece_bytes = 0;
+  c->pack_ctas_per_sm = 0;
+  c->pdl = 1;
+  *out = c;
+  return MOE_OK;
+}
+
+MOE_API int moe_ctx_destroy(moe_ctx* ctx) {
+  delete ctx;
+  return MOE_OK;
+}
+
+MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
+  if (!ctx) return MOE_EINVAL;
+  switch (option) {
+    case MOE_OPT_PACK_VARIANT:
+      if (value != moe::kPackBulk && value != moe::kPackVector) return MOE_EINVAL;
+      ctx->pack_variant = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_PACK_STAGES:
+      if (value < 2 || value > 8) return MOE_EINVAL;
+      ctx->pack_stages = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_PACK_PIECE_BYTES:
+      if (value < 0 || value % 16 != 0 || value > 65536) return MOE_EINVAL;
+      ctx->pack_piece_bytes = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_PACK_CTAS_PER_SM:
+      if (value < 0 || value > 32) return MOE_EINVAL;
+      ctx->pack_ctas_per_sm = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_PDL:
+      if (value != 0 && value != 1) return MOE_EINVAL;
+      ctx->pdl = static_cast<int>(value);
+      return MOE_OK;
+    default:
+      return MOE_EINVAL;
+  }
+}
+
+namespace {
+
+// Bytes per pack unit: the whole row when it is at most 16 KiB, else the
+// row split into equal 16-byte-multiple pieces of at most 16 KiB.
+int pack_piece_bytes(const moe_ctx* c, int64_t row_bytes) {
+  int64_t pb = c->pack_piece_bytes;
+  if (pb <= 0) {
+    const int64_t pieces = (row_bytes + 16384 - 1) / 16384;
+    pb = (row_bytes / 16 + pieces - 1) / pieces * 16;
+  }
+  if (pb > row_bytes) pb = row_bytes;
+  return static_cast<int>(pb);
+}
+
+int pack_grid(const moe_ctx* c, const moe::PackParams& p, int stages) {
+  const int64_t units = static_cast<int64_t>(p.T) * p.pieces;
+  int per_sm = c->pack_ctas_per_sm;
+  if (c->pack_variant == moe::kPackBulk) {
+    const size_t smem = moe::pack_bulk_smem_bytes(stages, p.piece_bytes);
+    // 228 KiB of shared memory per SM, 1 KiB of it reserved per resident CTA.
+    const int fit = static_cast<int>((228 * 1024) / (smem + 1024));
+    if (per_sm <= 0 || per_sm > fit) per_sm = fit;
+    if (per_sm < 1) per_sm = 1;
+  } else if (per_sm <= 0) {
+    per_sm = 8;  // 8 x 256 threads
+  }
+  int64_t grid = static_cast<int64_t>(c->num_sms) * per_sm;
+  const int64_t useful = c->pack_variant == moe::kPackBulk ? units : (units + 7) / 8;
+  if (grid > useful) grid = useful;
+  if (grid < 1) grid = 1;
+  return static_cast<int>(grid);
+}
+
+}  // namespace
+
+MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_x,
+                              int64_t expert_x_rows, void* stream) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->phase != kIdle) return MOE_ESTATE;
+  const moe_config& c = ctx->cfg;
+  const int64_t pairs = static_cast<int64_t>(c.num_tokens) * c.top_k;
+  if (expert_x_rows < pairs) return MOE_EINVAL;
+  if (c.num_tokens > 0) {
+    if (!x || !topk_idx || !expert_x) return MOE_EINVAL;
+    if (!aligned(x, 16) || !aligned(expert_x, 16) || !aligned(topk_idx, 4)) return MOE_EINVAL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  moe::RouteCountParams rp;
+  rp.topk_idx = topk_idx;
+  rp.T = c.num_tokens;
+  rp.K = c.top_k;
+  rp.E = c.num_experts;
+  rp.N = c.num_ranks;
+  rp.expert_counts = ctx->expert_counts;
+  rp.expert_offsets = ctx->expert_offsets;
+  rp.src_offsets = ctx->src_offsets;
+  rp.rank_offsets = ctx->rank_offsets;
+  rp.slot_row = ctx->slot_row;
+  rp.row_src = ctx->row_src;
+  rp.error_word = ctx->error_word;
+  int vec = 1;
+  if (c.top_k % 4 == 0 && aligned(topk_idx, 16)) vec = 4;
+  else if (c.top_k % 2 == 0 && aligned(topk_idx, 8)) vec = 2;
+  if (moe::launch_route_count(rp, vec, s) != cudaSuccess) return MOE_ECUDA;
+
+  if (c.num_tokens > 0) {
+    moe::PackParams pp;
+    pp.x = static_cast<const uint8_t*>(x);
+    pp.expert_x = static_cast<uint8_t*>(expert_x);
+    pp.slot_row = ctx->slot_row;
+    pp.error_word = ctx->error_word;
+    pp.T = c.num_tokens;
+    pp.K = c.top_k;
+    pp.row_bytes = static_cast<int64_t>(c.hidden) * 2;
+    pp.piece_bytes = pack_piece_bytes(ctx, pp.row_bytes);
+    pp.pieces = static_cast<int32_t>((pp.row_bytes + pp.piece_bytes - 1) / pp.piece_bytes);
+    moe::PackLaunch pl;
+    pl.variant = ctx->pack_variant;
+    pl.stages = ctx->pack_stages;
+    if (pl.variant == moe::kPackBulk) {
+      // Shrink the pipeline if the stages do not fit in one CTA's shared memory.
+      while (pl.stages > 2 &&
+             moe::pack_bulk_smem_bytes(pl.stages, pp.piece_bytes) > static_cast<size_t>(ctx->max_smem_optin))
+        --pl.stages;
+      if (moe::pack_bulk_smem_bytes(pl.stages, pp.piece_bytes) > static_cast<size_t>(ctx->max_smem_optin))
+        return MOE_EINVAL;
+    }
+    pl.grid = pack_grid(ctx, pp, pl.stages);
+    pl.pdl = ctx->pdl != 0;
+    if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
+  }
+  ctx->phase = kDispatched;
+  return MOE_OK;
+}
+
+MOE_API int moe_dispatch_recv(moe_ctx* ctx, moe_dispatch_layout* layout, void* stream) {
+  (void)stream;
+  if (!ctx || !layout) return MOE_EINVAL;
+  if (ctx->phase != kDispatched) return MOE_ESTATE;
+  layout->expert_counts = ctx->expert_counts;
+  layout->expert_offsets = ctx->expert_offsets;
+  layout->src_offsets = ctx->src_offsets;
+  layout->rank_offsets = ctx->rank_offsets;
+  layout->slot_row = ctx->slot_row;
+  layout->row_src = ctx->row_src;
+  layout->error_word = ctx->error_word;
+  layout->rows = static_cast<int64_t>(ctx->cfg.num_tokens) * ctx->cfg.top_k;
+  int64_t bound = 0;
+  moe_recv_bound_rows(&ctx->cfg, &bound);
+  layout->recv_bound_rows = bound;
+  ctx->phase = kReceived;
+  return MOE_OK;
+}
+
+MOE_API int moe_combine_send(moe_ctx* ctx, const void* expert_y, int64_t expert_y_rows, void* stream) {
+  (void)stream;
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->phase != kReceived) return MOE_ESTATE;
+  const moe_config& c = ctx->cfg;
+  if (expert_y_rows < static_cast<int64_t>(c.num_tokens) * c.top_k) return MOE_EINVAL;
+  if (c.num_tokens > 0 && (!expert_y || !aligned(expert_y, 16))) return MOE_EINVAL;
+  ctx->expert_y = expert_y;
+  ctx->expert_y_rows = expert_y_rows;
+  ctx->phase = kCombineSent;
+  return MOE_OK;
+}
+
+MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void* stream) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->phase != kCombineSent) return MOE_ESTATE;
+  const moe_config& c = ctx->cfg;
+  if (c.num_tokens > 0) {
+    if (!topk_w || !out || !aligned(topk_w, 4) || !aligned(out, 16)) return MOE_EINVAL;
+    moe::CombineParams cp;
+    cp.y = static_cast<const uint8_t*>(ctx->expert_y);
+    cp.w = topk_w;
+    cp.slot_row = ctx->slot_row;
+    cp.out = static_cast<uint8_t*>(out);
+    cp.T = c.num_tokens;
+    cp.K = c.top_k;
+    cp.H = c.hidden;
+    moe::CombineLaunch cl;
+    cl.pdl = ctx->pdl != 0;
+    if (moe::launch_combine(cp, cl, static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ECUDA;
+  }
+  ctx->expert_y = nullptr;
+  ctx->phase = kIdle;
+  return MOE_OK;
+}
+
+MOE_API int moe_get_error(moe_ctx* ctx, void* stream) {
+  if (!ctx) return MOE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t h = MOE_OK;
+  if (cudaMemcpyAsync(&h, ctx->error_word, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ECUDA;
+  return h;
+}
+
+MOE_API const char* moe_strerror(int status) {
+  switch (status) {
+    case MOE_OK:
+      return "ok";
+    case MOE_EINVAL:
+      return "invalid argument (null or misaligned pointer, or unsupported sizes)";
+    case MOE_ESTATE:
+      return "call out of order: dispatch_send -> dispatch_recv -> combine_send -> combine_recv";
+    case MOE_EROUTE:
+      return "expert index out of range or repeated within one token";
+    case MOE_ECUDA:
+      return "CUDA runtime or launch failure";
+    case MOE_EBOUND:
+      return "a logical rank would receive more rows than N*T/N*max(K,E/N)";
+    case MOE_ETIMEDOUT:
+      return "a bounded wait inside a kernel gave up";
+    default:
+      return "unknown status";
+  }
+}

@@ -1,0 +1,85 @@
+// Internal interface between the C ABI (moe_abi.cu) and the three kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <utility>
+
+#include "moe.h"
+
+namespace moe {
+
+// ---- route_count: counts, exclusive scan, stable slot ranks (one block) ----
+struct RouteCountParams {
+  const int32_t* topk_idx;  // [T, K]
+  int32_t T, K, E, N;
+  int32_t* expert_counts;   // [E]
+  int32_t* expert_offsets;  // [E+1]
+  int32_t* src_offsets;     // [E*N]
+  int32_t* rank_offsets;    // [N+1]
+  int32_t* slot_row;        // [T*K]
+  int32_t* row_src;         // [T*K]
+  int32_t* error_word;      // [1]
+};
+constexpr int kRouteThreads = 1024;
+// Dynamic shared memory the kernel needs for E experts.
+size_t route_count_smem_bytes(int E);
+// idx_vec: 4, 2 or 1 int32 per load (K % idx_vec == 0, topk_idx aligned to 4*idx_vec bytes).
+cudaError_t launch_route_count(const RouteCountParams& p, int idx_vec, cudaStream_t stream);
+
+// ---- dispatch_pack: expert_x[slot_row[t,k]] = x[t] --------------------------
+struct PackParams {
+  const uint8_t* x;         // [T, row_bytes]
+  uint8_t* expert_x;        // [rows, row_bytes]
+  const int32_t* slot_row;  // [T*K]
+  int32_t* error_word;
+  int32_t T, K;
+  int64_t row_bytes;        // H * 2, multiple of 16
+  int32_t piece_bytes;      // bytes moved per unit (multiple of 16, <= row_bytes)
+  int32_t pieces;           // ceil(row_bytes / piece_bytes)
+};
+enum PackVariant { kPackBulk = 0, kPackVector = 1 };
+struct PackLaunch {
+  int variant;    // PackVariant
+  int grid;       // CTAs
+  int stages;     // bulk: shared-memory stages per CTA (2..8)
+  bool pdl;       // launch with programmatic stream serialization
+};
+size_t pack_bulk_smem_bytes(int stages, int piece_bytes);
+cudaError_t prepare_pack(int max_smem_bytes);  // one-time per-device attribute setup
+cudaError_t launch_dispatch_pack(const PackParams& p, const PackLaunch& l, cudaStream_t stream);
+
+// ---- combine: out[t] = bf16(sum_k w[t,k] * y[slot_row[t,k]]) -----------------
+struct CombineParams {
+  const uint8_t* y;         // [rows, H] bf16
+  const float* w;           // [T, K]
+  const int32_t* slot_row;  // [T*K]
+  uint8_t* out;             // [T, H] bf16
+  int32_t T, K, H;
+};
+struct CombineLaunch {
+  bool pdl;  // launch with programmatic stream serialization
+};
+cudaError_t launch_combine(const CombineParams& p, const CombineLaunch& l, cudaStream_t stream);
+
+// Launch helper: plain or programmatic-dependent launch with cudaLaunchKernelEx.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace moe

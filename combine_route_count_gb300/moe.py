@@ -1,0 +1,252 @@
+"""Thin ctypes binding of libmoe.so (include/moe.h).
+
+Argument marshalling only: every step of dispatch and combine runs in the
+CUDA kernels behind the C ABI.  There is no CPU fallback: if the library is
+missing, every call raises.  Functions carry the C names; pointers may be
+given as integers or as torch tensors (their ``data_ptr()``), streams as
+integers, ``torch.cuda.Stream`` objects or ``None`` (torch's current stream).
+
+``MoELayer`` bundles one context with its torch-allocated workspace for the
+tests and the benchmark.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Any, Dict, Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe.so")
+
+MOE_OK, MOE_EINVAL, MOE_ESTATE, MOE_EROUTE, MOE_ECUDA, MOE_EBOUND, MOE_ETIMEDOUT = range(7)
+MOE_MAX_TOP_K = 16
+MOE_MAX_EXPERTS = 1024
+MOE_OPT_PACK_VARIANT, MOE_OPT_PACK_STAGES, MOE_OPT_PACK_PIECE_BYTES, MOE_OPT_PACK_CTAS_PER_SM, MOE_OPT_PDL = 1, 2, 3, 4, 5
+PACK_BULK, PACK_VECTOR = 0, 1
+
+# Every entry point of include/moe.h.
+EXPORTS = ("moe_validate_config", "moe_workspace_bytes", "moe_recv_bound_rows", "moe_ctx_create",
+           "moe_ctx_destroy", "moe_ctx_set_option", "moe_dispatch_send", "moe_dispatch_recv",
+           "moe_combine_send", "moe_combine_recv", "moe_get_error", "moe_strerror")
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("num_tokens", ctypes.c_int32), ("hidden", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("num_experts", ctypes.c_int32), ("num_ranks", ctypes.c_int32)]
+
+
+class moe_dispatch_layout(ctypes.Structure):
+    _fields_ = [("expert_counts", ctypes.c_void_p), ("expert_offsets", ctypes.c_void_p),
+                ("src_offsets", ctypes.c_void_p), ("rank_offsets", ctypes.c_void_p),
+                ("slot_row", ctypes.c_void_p), ("row_src", ctypes.c_void_p),
+                ("error_word", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("recv_bound_rows", ctypes.c_int64)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {moe_strerror(code)} (status {code})")
+        self.code = code
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libmoe.so; raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libmoe.so is not built ({path}); run __graft_entry__.build() "
+                           "or python combine_route_count_gb300/build.py")
+    lib = ctypes.CDLL(path)
+    P, I, I64, C = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.POINTER(moe_config)
+    sig = {
+        "moe_validate_config": ([C], I),
+        "moe_workspace_bytes": ([C, ctypes.POINTER(ctypes.c_size_t)], I),
+        "moe_recv_bound_rows": ([C, ctypes.POINTER(ctypes.c_int64)], I),
+        "moe_ctx_create": ([C, P, ctypes.c_size_t, ctypes.POINTER(P)], I),
+        "moe_ctx_destroy": ([P], I),
+        "moe_ctx_set_option": ([P, I, I64], I),
+        "moe_dispatch_send": ([P, P, P, P, I64, P], I),
+        "moe_dispatch_recv": ([P, ctypes.POINTER(moe_dispatch_layout), P], I),
+        "moe_combine_send": ([P, P, I64, P], I),
+        "moe_combine_recv": ([P, P, P, P], I),
+        "moe_get_error": ([P, P], I),
+        "moe_strerror": ([I], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _ptr(x: Any) -> Optional[int]:
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    return int(x)
+
+
+def _stream(s: Any) -> Optional[int]:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream) or None
+    if hasattr(s, "cuda_stream"):
+        return int(s.cuda_stream) or None
+    return int(s) or None
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != MOE_OK:
+        raise MoEError(rc, what)
+
+
+def make_config(T: int, H: int, K: int, E: int, N: int) -> moe_config:
+    return moe_config(T, H, K, E, N)
+
+
+# ---- the C entry points, same names ----------------------------------------
+
+def moe_validate_config(cfg: moe_config) -> int:
+    return load_library().moe_validate_config(ctypes.byref(cfg))
+
+
+def moe_workspace_bytes(cfg: moe_config) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().moe_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_bytes")
+    return int(n.value)
+
+
+def moe_recv_bound_rows(cfg: moe_config) -> int:
+    n = ctypes.c_int64(0)
+    _check(load_library().moe_recv_bound_rows(ctypes.byref(cfg), ctypes.byref(n)), "moe_recv_bound_rows")
+    return int(n.value)
+
+
+def moe_ctx_create(cfg: moe_config, workspace: Any, workspace_bytes: int) -> int:
+    h = ctypes.c_void_p(0)
+    _check(load_library().moe_ctx_create(ctypes.byref(cfg), _ptr(workspace), workspace_bytes, ctypes.byref(h)),
+           "moe_ctx_create")
+    return int(h.value)
+
+
+def moe_ctx_destroy(ctx: int) -> None:
+    _check(load_library().moe_ctx_destroy(ctx), "moe_ctx_destroy")
+
+
+def moe_ctx_set_option(ctx: int, option: int, value: int) -> None:
+    _check(load_library().moe_ctx_set_option(ctx, option, value), "moe_ctx_set_option")
+
+
+def moe_dispatch_send(ctx: int, x: Any, topk_idx: Any, expert_x: Any, expert_x_rows: int, stream: Any = None) -> None:
+    _check(load_library().moe_dispatch_send(ctx, _ptr(x), _ptr(topk_idx), _ptr(expert_x), expert_x_rows,
+                                            _stream(stream)), "moe_dispatch_send")
+
+
+def moe_dispatch_recv(ctx: int, stream: Any = None) -> moe_dispatch_layout:
+    lay = moe_dispatch_layout()
+    _check(load_library().moe_dispatch_recv(ctx, ctypes.byref(lay), _stream(stream)), "moe_dispatch_recv")
+    return lay
+
+
+def moe_combine_send(ctx: int, expert_y: Any, expert_y_rows: int, stream: Any = None) -> None:
+    _check(load_library().moe_combine_send(ctx, _ptr(expert_y), expert_y_rows, _stream(stream)), "moe_combine_send")
+
+
+def moe_combine_recv(ctx: int, topk_w: Any, out: Any, stream: Any = None) -> None:
+    _check(load_library().moe_combine_recv(ctx, _ptr(topk_w), _ptr(out), _stream(stream)), "moe_combine_recv")
+
+
+def moe_get_error(ctx: int, stream: Any = None) -> int:
+    return int(load_library().moe_get_error(ctx, _stream(stream)))
+
+
+def moe_strerror(code: int) -> str:
+    try:
+        return load_library().moe_strerror(code).decode()
+    except RuntimeError:
+        return f"status {code}"
+
+
+# ---- convenience: one context with a torch-allocated workspace ---------------
+
+class MoELayer:
+    """One dispatch+combine context on the current CUDA device.
+
+    Allocates the workspace with torch (the library itself allocates no
+    device memory) and exposes the four calls on torch tensors:
+    x bf16 [T, H], topk_idx int32 [T, K], expert_x bf16 [>= T*K, H],
+    expert_y bf16 [>= T*K, H], topk_w float32 [T, K], out bf16 [T, H].
+    """
+
+    def __init__(self, T: int, H: int, K: int, E: int, N: int, device: Any = None, **options: int):
+        import torch
+        self.cfg = make_config(T, H, K, E, N)
+        self.T, self.H, self.K, self.E, self.N = T, H, K, E, N
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        nbytes = moe_workspace_bytes(self.cfg)
+        with torch.cuda.device(self.device):
+            self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self.ctx = moe_ctx_create(self.cfg, self.workspace, self.workspace.numel())
+        names = {"pack_variant": MOE_OPT_PACK_VARIANT, "pack_stages": MOE_OPT_PACK_STAGES,
+                 "pack_piece_bytes": MOE_OPT_PACK_PIECE_BYTES, "pack_ctas_per_sm": MOE_OPT_PACK_CTAS_PER_SM,
+                 "pdl": MOE_OPT_PDL}
+        for k, v in options.items():
+            moe_ctx_set_option(self.ctx, names[k], int(v))
+
+    def close(self) -> None:
+        if getattr(self, "ctx", 0):
+            moe_ctx_destroy(self.ctx)
+            self.ctx = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def set_option(self, option: int, value: int) -> None:
+        moe_ctx_set_option(self.ctx, option, value)
+
+    def dispatch_send(self, x, topk_idx, expert_x, stream: Any = None) -> None:
+        moe_dispatch_send(self.ctx, x, topk_idx, expert_x, expert_x.shape[0], stream)
+
+    def dispatch_recv(self, stream: Any = None) -> Dict[str, Any]:
+        """Views (torch tensors into the workspace) of the dispatch layout."""
+        lay = moe_dispatch_recv(self.ctx, stream)
+        base = self.workspace.data_ptr()
+        i32 = self.workspace.view(__import__("torch").int32)
+
+        def view(ptr: int, n: int):
+            off = (ptr - base) // 4
+            return i32[off:off + n]
+
+        T, K, E, N = self.T, self.K, self.E, self.N
+        return {"expert_counts": view(lay.expert_counts, E), "expert_offsets": view(lay.expert_offsets, E + 1),
+                "src_offsets": view(lay.src_offsets, E * N).view(E, N),
+                "rank_offsets": view(lay.rank_offsets, N + 1),
+                "slot_row": view(lay.slot_row, T * K).view(T, K), "row_src": view(lay.row_src, T * K),
+                "error_word": view(lay.error_word, 1), "rows": int(lay.rows),
+                "recv_bound_rows": int(lay.recv_bound_rows)}
+
+    def combine_send(self, expert_y, stream: Any = None) -> None:
+        moe_combine_send(self.ctx, expert_y, expert_y.shape[0], stream)
+
+    def combine_recv(self, topk_w, out, stream: Any = None) -> None:
+        moe_combine_recv(self.ctx, topk_w, out, stream)
+
+    def get_error(self, stream: Any = None) -> int:
+        return moe_get_error(self.ctx, stream)
+
+    def layer(self, x, topk_idx, topk_w, expert_x, expert_y, out, stream: Any = None) -> Dict[str, Any]:
+        """dispatch_send -> dispatch_recv -> combine_send -> combine_recv."""
+        self.dispatch_send(x, topk_idx, expert_x, stream)
+        lay = self.dispatch_recv(stream)
+        self.combine_send(expert_y, stream)
+        self.combine_recv(topk_w, out, stream)
+        return lay

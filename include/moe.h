@@ -1,0 +1,179 @@
+/*
+ * moe.h - C ABI of the GB300 MoE dispatch + combine library (libmoe.so).
+ *
+ * One MoE layer on one GPU: tokens are routed to experts (dispatch), expert
+ * outputs are gathered back and reduced with the router weights (combine).
+ * "Ranks" are logical partitions of one GPU's memory: logical rank s owns
+ * tokens [s*T/N, (s+1)*T/N) and experts [r*E/N, (r+1)*E/N) live on rank r.
+ * Nothing crosses a GPU boundary.
+ *
+ * The four calls follow the split send/receive kernel pairs of
+ * "Efficient and portable mixture-of-experts communication" (Portable
+ * kernels; Dispatch; Combine) and "Enabling trillion-parameter models on AWS
+ * EFA" (Dispatch and combine: send halves pack, receive halves hand the
+ * grouped tensor to the grouped GEMM or compute the weighted average).
+ *
+ * Conventions for every call:
+ *  - Device pointers are plain CUDA device addresses owned by the caller; the
+ *    library allocates no device memory and keeps no global device state.
+ *    The only host allocation is the small moe_ctx handle.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call only enqueues work on that stream and returns
+ *    without waiting, except moe_get_error, which synchronises the stream.
+ *  - bf16 tensors are row-major, rows of H elements; x, expert_x, expert_y and
+ *    out must be 16-byte aligned (H must be a multiple of 8, so every row is).
+ *  - Return value: MOE_OK or one of the MOE_E* codes below.  Argument errors
+ *    are detected on the host before anything is enqueued.  Routing errors
+ *    (an expert index out of range or repeated within one token) are detected
+ *    on the device; they are reported by moe_get_error and by the error word
+ *    that moe_dispatch_recv exposes.  After a routing error no row of
+ *    expert_x and no row of out is written.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_EINVAL 1    /* bad argument: null/misaligned pointer, bad sizes */
+#define MOE_ESTATE 2    /* calls out of order for this context */
+#define MOE_EROUTE 3    /* device: expert index out of range or repeated in a token */
+#define MOE_ECUDA 4     /* a CUDA runtime call or a launch failed */
+#define MOE_EBOUND 5    /* device: a rank would receive more than N*T/N*max(K,E/N) rows */
+#define MOE_ETIMEDOUT 6 /* device: a bounded wait inside a kernel gave up */
+
+/* Limits of this implementation. */
+#define MOE_MAX_TOP_K 16
+#define MOE_MAX_EXPERTS 1024
+
+/* Sizes of one layer.  T % N == 0, E % N == 0, 1 <= K <= min(E, 16),
+ * E <= 1024, H % 8 == 0, T*K < 2^31.  T == 0 is allowed (an empty layer). */
+typedef struct moe_config {
+  int32_t num_tokens;  /* T: tokens over all logical ranks */
+  int32_t hidden;      /* H: bf16 elements per token row */
+  int32_t top_k;       /* K: experts per token */
+  int32_t num_experts; /* E */
+  int32_t num_ranks;   /* N: logical ranks */
+} moe_config;
+
+/* Opaque per-layer context: the configuration, the caller's workspace and
+ * the phase of the send/recv sequence. */
+typedef struct moe_ctx moe_ctx;
+
+/* Where dispatch put things.  All pointers are device pointers into the
+ * workspace, valid until the next moe_dispatch_send on the same context;
+ * their contents are ready in stream order after moe_dispatch_send.
+ *
+ * Row layout of expert_x (and of expert_y for combine): rows are grouped by
+ * expert, experts in index order, so the rows of logical rank r's experts are
+ * the contiguous range [rank_offsets[r], rank_offsets[r+1]).  Inside one
+ * expert, rows are ordered by source rank, then by token within the rank
+ * (equivalently, by global token index).  This placement is unique. */
+typedef struct moe_dispatch_layout {
+  const int32_t* expert_counts;  /* [E]   rows received by each expert */
+  const int32_t* expert_offsets; /* [E+1] first row of each expert; [E] = T*K */
+  const int32_t* src_offsets;    /* [E*N] first row of (expert e, source rank s) at e*N+s */
+  const int32_t* rank_offsets;   /* [N+1] first row of rank r's experts; [N] = T*K */
+  const int32_t* slot_row;       /* [T*K] row that token t's k-th choice went to, at t*K+k */
+  const int32_t* row_src;        /* [T*K] for each row, t*K+k of the (token, slot) it holds */
+  const int32_t* error_word;     /* [1]   MOE_OK or the device-detected status */
+  int64_t rows;                  /* T*K: rows written at the front of expert_x */
+  int64_t recv_bound_rows;       /* N*(T/N)*max(K, E/N): most rows one rank can receive */
+} moe_dispatch_layout;
+
+/* Checks a configuration against the limits above.  MOE_OK or MOE_EINVAL. */
+int moe_validate_config(const moe_config* cfg);
+
+/* Device workspace (bytes, a multiple of 256) that one context needs: counts,
+ * offsets, slot_row, row_src and the error word.  Allocate it 256-byte
+ * aligned; its contents need no initialisation. */
+int moe_workspace_bytes(const moe_config* cfg, size_t* bytes);
+
+/* The receive bound of "Enabling trillion-parameter models on AWS EFA"
+ * (Send and receive buffers): with N ranks of T/N tokens each routed to K of
+ * E experts, one rank receives at most N*(T/N)*max(K, E/N) rows. */
+int moe_recv_bound_rows(const moe_config* cfg, int64_t* rows);
+
+/* Creates a context over a caller-owned device workspace of at least
+ * moe_workspace_bytes() bytes.  Must be called with the device that owns the
+ * workspace current; all later calls must use a stream of that device.
+ * The context is not thread-safe: one host thread drives one context. */
+int moe_ctx_create(const moe_config* cfg, void* workspace, size_t workspace_bytes, moe_ctx** out);
+
+/* Frees the host handle (not the workspace). NULL is a no-op. */
+int moe_ctx_destroy(moe_ctx* ctx);
+
+/* Dispatch, send half ("Enabling trillion-parameter models on AWS EFA",
+ * Dispatch and combine: count tokens per expert with shared-memory atomics in
+ * one block, take the cumulative sum of the counts, pack the tokens at those
+ * offsets).  Enqueues route_count (one block: counts, exclusive scan,
+ * stable slot ranks, routing error check) and dispatch_pack (copies each
+ * token row x[t] to expert_x[slot_row[t,k]] for every k).
+ *   x         device bf16 [T, H], read only
+ *   topk_idx  device int32 [T, K], read only, 4-byte aligned
+ *   expert_x  device bf16 [expert_x_rows, H]; rows [0, T*K) are written,
+ *             later rows are left untouched.  expert_x_rows >= T*K.
+ * Valid in the idle phase (after create or after moe_combine_recv). */
+int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_x,
+                      int64_t expert_x_rows, void* stream);
+
+/* Dispatch, receive half.  On one GPU the send half already placed every row
+ * in the grouped layout (the shared-buffer case of "Efficient and portable
+ * mixture-of-experts communication", Further improvements), so this enqueues
+ * nothing: it fills `layout` with device pointers to the counts, offsets and
+ * routing tables.  Valid after moe_dispatch_send. */
+int moe_dispatch_recv(moe_ctx* ctx, moe_dispatch_layout* layout, void* stream);
+
+/* Combine, send half: registers the expert outputs, one row per dispatched
+ * (token, slot) pair in the same row layout as expert_x.  Nothing is copied
+ * (the senders' per-expert regions are this GPU's own memory).
+ *   expert_y  device bf16 [expert_y_rows, H], expert_y_rows >= T*K
+ * Valid after moe_dispatch_recv. */
+int moe_combine_send(moe_ctx* ctx, const void* expert_y, int64_t expert_y_rows, void* stream);
+
+/* Combine, receive half ("Efficient and portable mixture-of-experts
+ * communication", Combine: the weighted average of all expert contributions,
+ * computed where the token lives, into a caller-allocated tensor).  Enqueues
+ * the combine kernel:
+ *   out[t, h] = bf16_rne( fma chain over k = 0..K-1 of
+ *                         topk_w[t, k] * expert_y[slot_row[t, k], h], from +0.0f )
+ * accumulated in float32 in top-k order, rounded once to bf16 (nearest even).
+ *   topk_w  device float32 [T, K], 4-byte aligned
+ *   out     device bf16 [T, H]
+ * Valid after moe_combine_send; returns the context to the idle phase. */
+int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void* stream);
+
+/* Launch options of one context (tuning knobs; the defaults are the tuned
+ * configuration).  Returns MOE_EINVAL for an unknown option or value.
+ *   MOE_OPT_PACK_VARIANT      0 = bulk copies through shared memory (TMA
+ *                             engine, default), 1 = 16-byte vector loads/stores
+ *   MOE_OPT_PACK_STAGES       shared-memory stages per bulk CTA, 2..8 (default 4)
+ *   MOE_OPT_PACK_PIECE_BYTES  bytes of a row moved per work unit, a multiple of
+ *                             16, 0 = automatic (whole row up to 16 KiB)
+ *   MOE_OPT_PACK_CTAS_PER_SM  0 = as many as fit, else 1..32
+ *   MOE_OPT_PDL               1 = launch pack/combine with programmatic
+ *                             dependent launch (default), 0 = plain launches */
+#define MOE_OPT_PACK_VARIANT 1
+#define MOE_OPT_PACK_STAGES 2
+#define MOE_OPT_PACK_PIECE_BYTES 3
+#define MOE_OPT_PACK_CTAS_PER_SM 4
+#define MOE_OPT_PDL 5
+int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
+
+/* Synchronises `stream` and returns the device status of the last dispatch
+ * (MOE_OK, MOE_EROUTE, MOE_EBOUND or MOE_ETIMEDOUT), or MOE_ECUDA. */
+int moe_get_error(moe_ctx* ctx, void* stream);
+
+/* Static description of a status code. */
+const char* moe_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,294 @@
+"""GPU path vs the CPU oracle, through the C ABI (libmoe.so).
+
+Bar: dispatch outputs (grouped rows, counts, offsets, slot_row, row_src) are
+compared bit for bit; the combine output is compared bit for bit against the
+oracle's float32 chain (fixed top-k order, one fused multiply-add per expert,
+one round-to-nearest-even), and in addition must stay within one bf16 ulp of
+the double-precision sum except where the float32 sum cancels (bounded by the
+float32 accumulation error, see the oracle pins).
+
+Covers the five named workloads at full size in the launch configuration the
+benchmark uses, every pack variant and launch option, ragged and degenerate
+shapes, routing errors and the call-order state machine.  Guard rows around
+every output catch stray writes.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+from combine_route_count_gb300 import inputs as gen  # noqa: E402
+
+GUARD = 3
+CANARY = 0x7BCD  # a bf16 bit pattern no input row is expected to hold everywhere
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from combine_route_count_gb300 import build, moe as m
+    build.build()
+    m.load_library()
+    return m
+
+
+def _dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.cuda()
+
+
+def _guarded(rows, H):
+    """A [GUARD + rows + GUARD, H] int16 canary buffer and its middle view."""
+    big = torch.full((GUARD + rows + GUARD, H), CANARY, dtype=torch.int16, device="cuda")
+    return big, big[GUARD:GUARD + rows]
+
+
+def _intact(big, rows):
+    v = big.cpu().numpy().view(np.uint16)
+    return bool(np.all(v[:GUARD] == CANARY) and np.all(v[GUARD + rows:] == CANARY))
+
+
+def run_gpu(moe, w, li, extra_rows=0, stream=None, **options):
+    T, H, K, E, N = w.T, w.H, w.K, w.E, w.N
+    rows = T * K
+    x = _dev(li.x.view(np.int16))
+    idx = _dev(li.topk_idx)
+    wt = _dev(li.topk_w)
+    y = _dev(li.y.view(np.int16)) if li.y is not None else torch.zeros((rows, H), dtype=torch.int16, device="cuda")
+    ex_big, expert_x = _guarded(rows + extra_rows, H)
+    out_big, out = _guarded(T, H)
+    layer = moe.MoELayer(T, H, K, E, N, **options)
+    lay = layer.layer(x, idx, wt, expert_x, y, out, stream)
+    status = layer.get_error(stream)
+    torch.cuda.synchronize()
+    res = {k: (v.cpu().numpy() if hasattr(v, "cpu") else v) for k, v in lay.items()}
+    res.update(status=status, expert_x=expert_x.cpu().numpy().view(np.uint16), out=out.cpu().numpy().view(np.uint16),
+               guards_ok=_intact(ex_big, rows + extra_rows) and _intact(out_big, T), layer=layer)
+    return res
+
+
+_oracle_cache = {}
+
+
+def oracle_of(oracle_mod, w, li):
+    key = (w.name, w.T, w.H, w.K, w.E, w.N, w.index)
+    if key not in _oracle_cache:
+        d = oracle_mod.dispatch(li.x, li.topk_idx, w.E, w.N)
+        out = oracle_mod.combine(li.y, li.topk_w, d.slot_row)
+        _oracle_cache.clear()
+        _oracle_cache[key] = (d, out)
+    return _oracle_cache[key]
+
+
+def assert_parity(res, d, out_ref, w, extra_rows=0):
+    rows = w.T * w.K
+    assert res["status"] == 0
+    assert res["guards_ok"], "a write landed outside an output buffer"
+    assert np.array_equal(res["expert_counts"], d.expert_counts)
+    assert np.array_equal(res["expert_offsets"], d.expert_offsets)
+    assert np.array_equal(res["rank_offsets"], d.rank_offsets)
+    assert np.array_equal(res["src_offsets"], d.src_offsets)
+    assert np.array_equal(res["slot_row"], d.slot_row)
+    assert np.array_equal(res["row_src"], d.row_src)
+    assert np.array_equal(res["expert_x"][:rows], d.expert_x[:rows])
+    if extra_rows:
+        assert np.all(res["expert_x"][rows:] == CANARY), "rows past T*K must stay untouched"
+    assert np.array_equal(res["out"], out_ref)
+
+
+@pytest.mark.parametrize("name", [w.name for w in gen.WORKLOADS])
+def test_named_workload_full_size(moe, oracle_mod, name):
+    w = gen.BY_NAME[name]
+    li = gen.make_inputs(w)
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    res = run_gpu(moe, w, li)
+    assert_parity(res, d, out_ref, w)
+    assert res["recv_bound_rows"] == w.N * w.tokens_per_rank * max(w.K, w.E // w.N)
+    if name == "worst":
+        recv = np.diff(res["rank_offsets"])
+        assert recv[0] == res["recv_bound_rows"] == 65536 and np.all(recv[1:] == 0)
+    # combine within one bf16 step of the double-precision sum wherever the
+    # float32 chain does not cancel (sampled rows: the f64 oracle is slower)
+    sample = np.random.default_rng(0).choice(w.T, size=min(w.T, 64), replace=False)
+    sub_w = li.topk_w[sample]
+    sub_slot = d.slot_row[sample]
+    o64, exact, mag = oracle_mod.combine_f64(li.y, sub_w, sub_slot)
+    gpu = res["out"][sample]
+    step = np.abs(gpu.astype(np.int32) - o64.astype(np.int32))
+    assert np.mean(step <= 1) > 0.999
+    g = gen.bf16_bits_to_f32(gpu).astype(np.float64)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(g), 2.0 ** -126))) - 7)
+    assert np.all(np.abs(g - exact) <= w.K * 2.0 ** -24 * mag * 1.001 + 0.5 * ulp + 1e-30)
+
+
+def test_identity_experts_return_the_input(moe):
+    """y = expert_x (identity experts) with weights summing to one gives x."""
+    w = gen.BY_NAME["deepseek"]
+    li = gen.make_inputs(gen.Workload("ds-id", T=1024, H=w.H, K=w.K, E=w.E, N=8, router=w.router, index=w.index),
+                         with_y=False)
+    T, H, K = 1024, w.H, w.K
+    x = _dev(li.x.view(np.int16))
+    idx = _dev(li.topk_idx)
+    wt = _dev(li.topk_w)
+    expert_x = torch.empty((T * K, H), dtype=torch.int16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    layer = moe.MoELayer(T, H, K, w.E, 8)
+    layer.layer(x, idx, wt, expert_x, expert_x, out)
+    assert layer.get_error() == 0
+    assert torch.equal(out, x)
+
+
+PACK_OPTIONS = [
+    dict(pack_variant=0, pack_stages=2),
+    dict(pack_variant=0, pack_stages=8, pack_piece_bytes=2048),
+    dict(pack_variant=0, pack_stages=3, pack_piece_bytes=4096 + 512, pack_ctas_per_sm=1),
+    dict(pack_variant=0, pdl=0),
+    dict(pack_variant=1),
+    dict(pack_variant=1, pack_piece_bytes=1024, pdl=0),
+]
+
+
+@pytest.mark.parametrize("opts", PACK_OPTIONS, ids=[str(o) for o in PACK_OPTIONS])
+def test_launch_options_give_identical_results(moe, oracle_mod, opts):
+    w = gen.custom("opts", T=2 * 1000, H=7168, K=8, E=256, N=8, router="uniform_random", seed_index=7)
+    li = gen.make_inputs(w)
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    res = run_gpu(moe, w, li, **opts)
+    assert_parity(res, d, out_ref, w)
+
+
+EDGE = [
+    # (T, H, K, E, N, router)
+    (1, 8, 1, 1, 1, "uniform_random"),          # one token, one expert, narrowest row
+    (3, 24, 3, 3, 1, "uniform_random"),         # E == K, odd K (scalar index loads)
+    (6, 40, 1, 6, 6, "uniform_random"),         # one token per rank, E == N
+    (1000, 136, 5, 40, 4, "uniform_random"),    # ragged chunk, odd K, rows not a power of two
+    (2049, 64, 2, 6, 3, "uniform_random"),      # chunks of 1024 + tail of 1
+    (512, 256, 16, 64, 4, "uniform_random"),    # K = 16 (max)
+    (1024, 128, 7, 1024, 8, "uniform_random"),  # E = 1024 (max): 512-token chunks
+    (1540, 64, 4, 770, 2, "uniform_random"),    # E > 768 path, ragged
+    (64, 8200, 2, 8, 2, "uniform_random"),      # row > 16 KiB: split into pieces
+    (4096, 2056, 6, 96, 16, "uniform_random"),  # odd-ish row bytes (4112)
+    (8192, 64, 8, 64, 8, "rank0_only"),         # everything to rank 0
+]
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=["x".join(map(str, s[:5])) for s in EDGE])
+def test_edge_shapes(moe, oracle_mod, shape):
+    T, H, K, E, N, router = shape
+    w = gen.custom("edge", T=T, H=H, K=K, E=E, N=N, router=router, seed_index=11)
+    li = gen.make_inputs(w)
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    res = run_gpu(moe, w, li, extra_rows=5)
+    assert_parity(res, d, out_ref, w, extra_rows=5)
+
+
+def test_empty_layer(moe):
+    layer = moe.MoELayer(0, 64, 2, 8, 2)
+    x = torch.empty((0, 64), dtype=torch.int16, device="cuda")
+    idx = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    wt = torch.empty((0, 2), dtype=torch.float32, device="cuda")
+    big, ex = _guarded(0, 64)
+    lay = layer.layer(x, idx, wt, ex, ex, x)
+    assert layer.get_error() == 0
+    assert lay["expert_counts"].cpu().tolist() == [0] * 8
+    assert lay["expert_offsets"].cpu().tolist() == [0] * 9
+    assert lay["src_offsets"].cpu().numpy().tolist() == [[0, 0]] * 8
+    assert _intact(big, 0)
+
+
+def test_non_default_stream_and_reuse(moe, oracle_mod):
+    """Two layers back to back on a side stream reuse one context and workspace."""
+    s = torch.cuda.Stream()
+    for seed in (21, 22):
+        w = gen.custom("stream", T=512, H=512, K=4, E=32, N=4, seed_index=seed)
+        li = gen.make_inputs(w)
+        d, out_ref = oracle_of(oracle_mod, w, li)
+        with torch.cuda.stream(s):
+            res = run_gpu(moe, w, li, stream=s)
+        assert_parity(res, d, out_ref, w)
+
+
+@pytest.mark.parametrize("bad", ["out_of_range", "negative", "repeated"])
+def test_routing_errors_write_nothing(moe, bad):
+    w = gen.custom("bad", T=300, H=64, K=4, E=16, N=4, seed_index=3)
+    li = gen.make_inputs(w)
+    idx = li.topk_idx.copy()
+    if bad == "out_of_range":
+        idx[123, 2] = 16
+    elif bad == "negative":
+        idx[7, 0] = -1
+    else:
+        idx[299, 3] = idx[299, 1]
+    li2 = gen.LayerInputs(w, li.x, idx, li.topk_w, li.y)
+    res = run_gpu(moe, w, li2)
+    assert res["status"] == moe.MOE_EROUTE
+    assert res["error_word"][0] == moe.MOE_EROUTE
+    assert res["guards_ok"]
+    assert np.all(res["expert_x"] == CANARY)
+    assert np.all(res["out"] == CANARY)
+    assert np.all(res["slot_row"] == -1)
+    # the same context then runs a valid layer normally
+    layer = res["layer"]
+    T, H, K = w.T, w.H, w.K
+    x = _dev(li.x.view(np.int16))
+    ex = torch.empty((T * K, H), dtype=torch.int16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    layer.layer(x, _dev(li.topk_idx), _dev(li.topk_w), ex, _dev(li.y.view(np.int16)), out)
+    assert layer.get_error() == moe.MOE_OK
+
+
+def test_call_order_and_argument_checks(moe):
+    T, H, K, E, N = 64, 64, 2, 8, 2
+    layer = moe.MoELayer(T, H, K, E, N)
+    x = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    idx = torch.tensor([[t % E, (t + 1) % E] for t in range(T)], dtype=torch.int32, device="cuda")
+    wt = torch.full((T, K), 0.5, dtype=torch.float32, device="cuda")
+    ex = torch.zeros((T * K, H), dtype=torch.int16, device="cuda")
+    out = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    with pytest.raises(moe.MoEError) as ei:
+        layer.dispatch_recv()
+    assert ei.value.code == moe.MOE_ESTATE
+    with pytest.raises(moe.MoEError) as ei:
+        layer.combine_recv(wt, out)
+    assert ei.value.code == moe.MOE_ESTATE
+    # too few rows, misaligned pointer
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_dispatch_send(layer.ctx, x, idx, ex, T * K - 1)
+    assert ei.value.code == moe.MOE_EINVAL
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_dispatch_send(layer.ctx, x.data_ptr() + 2, idx, ex, T * K)
+    assert ei.value.code == moe.MOE_EINVAL
+    layer.dispatch_send(x, idx, ex)
+    with pytest.raises(moe.MoEError) as ei:
+        layer.dispatch_send(x, idx, ex)
+    assert ei.value.code == moe.MOE_ESTATE
+    layer.dispatch_recv()
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_combine_send(layer.ctx, ex, T * K - 1)
+    assert ei.value.code == moe.MOE_EINVAL
+    layer.combine_send(ex)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_combine_recv(layer.ctx, wt, out.data_ptr() + 8)
+    assert ei.value.code == moe.MOE_EINVAL
+    layer.combine_recv(wt, out)
+    assert layer.get_error() == moe.MOE_OK
+    for opt, val in [(moe.MOE_OPT_PACK_STAGES, 1), (moe.MOE_OPT_PACK_VARIANT, 5),
+                     (moe.MOE_OPT_PACK_PIECE_BYTES, 24), (99, 0)]:
+        with pytest.raises(moe.MoEError):
+            layer.set_option(opt, val)
+
+
+def test_repeat_runs_are_byte_identical(moe):
+    w = gen.custom("det", T=2048, H=1024, K=8, E=64, N=8, seed_index=5)
+    li = gen.make_inputs(w)
+    first = run_gpu(moe, w, li)
+    for _ in range(3):
+        again = run_gpu(moe, w, li)
+        for k in ("expert_x", "out", "slot_row", "row_src", "expert_offsets", "src_offsets"):
+            assert np.array_equal(first[k], again[k]), k
