@@ -27,7 +27,8 @@ PACK_BULK, PACK_VECTOR = 0, 1
 # Every entry point of include/moe.h.
 EXPORTS = ("moe_validate_config", "moe_workspace_bytes", "moe_recv_bound_rows", "moe_ctx_create",
            "moe_ctx_destroy", "moe_ctx_set_option", "moe_dispatch_send", "moe_dispatch_recv",
-           "moe_combine_send", "moe_combine_recv", "moe_get_error", "moe_strerror")
+           "moe_combine_send", "moe_combine_recv", "moe_get_error", "moe_strerror",
+           "moe_dispatch_send_noalloc")
 
 
 class moe_config(ctypes.Structure):
@@ -171,6 +172,25 @@ def moe_strerror(code: int) -> str:
         return load_library().moe_strerror(code).decode()
     except RuntimeError:
         return f"status {code}"
+
+
+MOE_NOALLOC_MAX_PAIRS = 262144
+MOE_NOALLOC_MAX_EXPERT_RANKS = 65536
+MOE_NOALLOC_SCRATCH_BYTES = 2363648
+
+
+def moe_dispatch_send_noalloc(cfg: moe_config, x: Any, topk_idx: Any, expert_x: Any, expert_x_rows: int,
+                              expert_counts: Any, expert_offsets: Any, status: Any, stream: Any = None) -> int:
+    """Dispatch for callers that cannot allocate device memory: the routing
+    tables live in the library's static device array instead of a workspace.
+    Returns the C status code (MOE_EINVAL for sizes beyond the array)."""
+    fn = load_library().moe_dispatch_send_noalloc
+    if fn.argtypes is None:
+        P = ctypes.c_void_p
+        fn.argtypes = [ctypes.POINTER(moe_config), P, P, P, ctypes.c_int64, P, P, P, P]
+        fn.restype = ctypes.c_int
+    return int(fn(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(expert_x), expert_x_rows, _ptr(expert_counts),
+                  _ptr(expert_offsets), _ptr(status), _stream(stream)))
 
 
 # ---- convenience: one context with a torch-allocated workspace ---------------

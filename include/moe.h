@@ -165,6 +165,37 @@ int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void* stream)
 #define MOE_OPT_PDL 5
 int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
 
+/* ---- Dispatch without any device allocation ------------------------------
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot call cudaMalloc (code running inside another framework's memory
+ * pool without an allocator handle, allocation-free runtime sections,
+ * processes that may not grow their device footprint after start-up), so
+ * they cannot provide the workspace that moe_ctx_create needs.
+ *
+ * Does what moe_dispatch_send does (route_count + dispatch_pack, same
+ * kernels, same results) but keeps the routing tables in one fixed static
+ * device array inside the library (MOE_NOALLOC_SCRATCH_BYTES, held by every
+ * GPU that loads libmoe.so until the process exits) and allocates nothing.
+ *   x, topk_idx, expert_x, expert_x_rows  as for moe_dispatch_send
+ *   expert_counts   device int32 [E], written
+ *   expert_offsets  device int32 [E+1], written
+ *   status          device int32 [1], written: MOE_OK or the device-detected
+ *                   status (MOE_EROUTE, MOE_EBOUND, MOE_ETIMEDOUT)
+ * Returns MOE_EINVAL, before enqueuing anything, when T*K exceeds
+ * MOE_NOALLOC_MAX_PAIRS or E*N exceeds MOE_NOALLOC_MAX_EXPERT_RANKS, or for
+ * the argument errors of moe_dispatch_send; MOE_ECUDA on a CUDA failure.
+ * The first call on a device (with that device current) looks up the static
+ * array's device address and sets kernel attributes; make that first call
+ * before any stream capture.  All calls share the array: calls whose kernels
+ * may overlap on the GPU (unordered streams, several host threads) race.
+ * No context is involved; there is no combine counterpart. */
+#define MOE_NOALLOC_MAX_PAIRS 262144
+#define MOE_NOALLOC_MAX_EXPERT_RANKS 65536
+#define MOE_NOALLOC_SCRATCH_BYTES 2363648
+int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, const int32_t* topk_idx, void* expert_x,
+                              int64_t expert_x_rows, int32_t* expert_counts, int32_t* expert_offsets,
+                              int32_t* status, void* stream);
+
 /* Synchronises `stream` and returns the device status of the last dispatch
  * (MOE_OK, MOE_EROUTE, MOE_EBOUND or MOE_ETIMEDOUT), or MOE_ECUDA. */
 int moe_get_error(moe_ctx* ctx, void* stream);
