@@ -333,7 +333,10 @@ def run_gpu(args):
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": f"inputs > L2: {ab['total'] / 1e6:.0f} MB moved per layer, "
                              f"{args.buffer_sets} rotating buffer sets",
-                       "pack": "bulk (TMA) 4 stages, PDL"},
+                       "pack": "bulk (TMA) 4 stages, PDL",
+                       "routing": {1: "route_count (1 block)", 2: "route_local+route_finalize",
+                                   3: f"route_cluster ({layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS)} CTAs)"}[
+                           layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)]},
             "achieved_gbs": round(ab["total"] / us_layer / 1e3, 1),
             "hbm_frac": round(ab["total"] / us_layer / 1e3 / peak, 4),
             "algorithmic_bytes_per_layer": ab["total"],
@@ -343,7 +346,7 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clk,
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": layer.kernels_per_layer() * args.steps,
         }
         print(json.dumps(line), flush=True)
     layer.close()

@@ -31,7 +31,8 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct WorkspaceLayout {
-  size_t error_word, expert_counts, expert_offsets, src_offsets, rank_offsets, slot_row, row_src, total;
+  size_t error_word, expert_counts, expert_offsets, src_offsets, rank_offsets, slot_row, row_src, hist, block_err,
+      total;
 };
 
 WorkspaceLayout layout_of(const moe_config& c) {
@@ -52,6 +53,10 @@ WorkspaceLayout layout_of(const moe_config& c) {
   o += align_up(sizeof(int32_t) * pairs);
   l.row_src = o;
   o += align_up(sizeof(int32_t) * pairs);
+  l.hist = o;  // per-chunk expert histograms of the split routing kernels
+  o += align_up(sizeof(int32_t) * static_cast<size_t>(moe::kMaxSplitBlocks) * c.num_experts);
+  l.block_err = o;
+  o += align_up(sizeof(int32_t) * moe::kMaxSplitBlocks);
   l.total = o;
   return l;
 }
@@ -77,12 +82,18 @@ struct moe_ctx {
   int32_t* rank_offsets;
   int32_t* slot_row;
   int32_t* row_src;
+  int32_t* hist;
+  int32_t* block_err;
   // launch options (MOE_OPT_* in moe.h)
   int pack_variant;
   int pack_stages;
   int pack_piece_bytes;  // 0 = automatic
   int pack_ctas_per_sm;  // 0 = as many as fit
   int pdl;
+  int route_variant;  // MOE_OPT_ROUTE_VARIANT
+  int cluster_ctas;   // route_cluster shape for this configuration (0 = cannot be scheduled)
+  int cluster_chunk;
+  int cluster_warps;
 };
 
 MOE_API int moe_validate_config(const moe_config* c) {
@@ -128,6 +139,7 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ECUDA;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return MOE_ECUDA;
   if (moe::route_count_smem_bytes(cfg->num_experts) > static_cast<size_t>(optin)) return MOE_EINVAL;
+  if (moe::route_local_smem_bytes(cfg->num_experts) > static_cast<size_t>(optin)) return MOE_EINVAL;
   if (moe::prepare_pack(optin) != cudaSuccess) return MOE_ECUDA;
 
   moe_ctx* c = new (std::nothrow) moe_ctx;
@@ -147,11 +159,34 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->rank_offsets = reinterpret_cast<int32_t*>(c->ws + l.rank_offsets);
   c->slot_row = reinterpret_cast<int32_t*>(c->ws + l.slot_row);
   c->row_src = reinterpret_cast<int32_t*>(c->ws + l.row_src);
+  c->hist = reinterpret_cast<int32_t*>(c->ws + l.hist);
+  c->block_err = reinterpret_cast<int32_t*>(c->ws + l.block_err);
   c->pack_variant = moe::kPackBulk;
   c->pack_stages = 4;
   c->pack_piece_bytes = 0;
   c->pack_ctas_per_sm = 0;
   c->pdl = 1;
+  c->route_variant = 0;
+  // Largest cluster of route_cluster CTAs this device can schedule for this
+  // configuration (16, else 8, 4, 2, 1), or none.
+  for (int maxc = moe::kMaxClusterCtas; maxc >= 1; maxc /= 2) {
+    int ctas = 0, chunk = 0, warps = 0;
+    moe::route_cluster_shape(cfg->num_tokens, cfg->num_experts, maxc, &ctas, &chunk, &warps);
+    if (moe::route_cluster_smem_bytes(cfg->num_experts, warps) > static_cast<size_t>(optin)) continue;
+    moe::RouteClusterParams q = {};
+    q.T = cfg->num_tokens;
+    q.K = cfg->top_k;
+    q.E = cfg->num_experts;
+    q.N = cfg->num_ranks;
+    q.chunk = chunk;
+    q.warps = warps;
+    if (moe::route_cluster_supported(q, 1, ctas)) {
+      c->cluster_ctas = ctas;
+      c->cluster_chunk = chunk;
+      c->cluster_warps = warps;
+      break;
+    }
+  }
   *out = c;
   return MOE_OK;
 }
@@ -183,6 +218,40 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
     case MOE_OPT_PDL:
       if (value != 0 && value != 1) return MOE_EINVAL;
       ctx->pdl = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_ROUTE_VARIANT:
+      if (value < 0 || value > 3) return MOE_EINVAL;
+      if (value == 3 && ctx->cluster_ctas == 0) return MOE_EINVAL;
+      ctx->route_variant = static_cast<int>(value);
+      return MOE_OK;
+    default:
+      return MOE_EINVAL;
+  }
+}
+
+MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
+  if (!ctx || !value) return MOE_EINVAL;
+  switch (option) {
+    case MOE_OPT_PACK_VARIANT:
+      *value = ctx->pack_variant;
+      return MOE_OK;
+    case MOE_OPT_PACK_STAGES:
+      *value = ctx->pack_stages;
+      return MOE_OK;
+    case MOE_OPT_PACK_PIECE_BYTES:
+      *value = ctx->pack_piece_bytes;
+      return MOE_OK;
+    case MOE_OPT_PACK_CTAS_PER_SM:
+      *value = ctx->pack_ctas_per_sm;
+      return MOE_OK;
+    case MOE_OPT_PDL:
+      *value = ctx->pdl;
+      return MOE_OK;
+    case MOE_OPT_ROUTE_VARIANT:
+      *value = ctx->route_variant != 0 ? ctx->route_variant : (ctx->cluster_ctas > 0 ? 3 : 2);
+      return MOE_OK;
+    case MOE_OPT_ROUTE_CLUSTER_CTAS:
+      *value = ctx->cluster_ctas;
       return MOE_OK;
     default:
       return MOE_EINVAL;
@@ -253,7 +322,45 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
   int vec = 1;
   if (c.top_k % 4 == 0 && aligned(topk_idx, 16)) vec = 4;
   else if (c.top_k % 2 == 0 && aligned(topk_idx, 8)) vec = 2;
-  if (moe::launch_route_count(rp, vec, s) != cudaSuccess) return MOE_ECUDA;
+  const bool use_cluster = (ctx->route_variant == 0 || ctx->route_variant == 3) && ctx->cluster_ctas > 0;
+  if (ctx->route_variant == 1) {
+    if (moe::launch_route_count(rp, vec, s) != cudaSuccess) return MOE_ECUDA;
+  } else if (use_cluster) {
+    moe::RouteClusterParams cp;
+    cp.topk_idx = topk_idx;
+    cp.T = c.num_tokens;
+    cp.K = c.top_k;
+    cp.E = c.num_experts;
+    cp.N = c.num_ranks;
+    cp.chunk = ctx->cluster_chunk;
+    cp.warps = ctx->cluster_warps;
+    cp.expert_counts = ctx->expert_counts;
+    cp.expert_offsets = ctx->expert_offsets;
+    cp.src_offsets = ctx->src_offsets;
+    cp.rank_offsets = ctx->rank_offsets;
+    cp.slot_row = ctx->slot_row;
+    cp.row_src = ctx->row_src;
+    cp.error_word = ctx->error_word;
+    if (moe::launch_route_cluster(cp, vec, ctx->cluster_ctas, s) != cudaSuccess) return MOE_ECUDA;
+  } else {
+    moe::RouteSplitParams sp;
+    sp.topk_idx = topk_idx;
+    sp.T = c.num_tokens;
+    sp.K = c.top_k;
+    sp.E = c.num_experts;
+    sp.N = c.num_ranks;
+    sp.chunk = moe::route_split_chunk(c.num_tokens);
+    sp.expert_counts = ctx->expert_counts;
+    sp.expert_offsets = ctx->expert_offsets;
+    sp.src_offsets = ctx->src_offsets;
+    sp.rank_offsets = ctx->rank_offsets;
+    sp.slot_row = ctx->slot_row;
+    sp.row_src = ctx->row_src;
+    sp.error_word = ctx->error_word;
+    sp.hist = ctx->hist;
+    sp.block_err = ctx->block_err;
+    if (moe::launch_route_split(sp, vec, s) != cudaSuccess) return MOE_ECUDA;
+  }
 
   if (c.num_tokens > 0) {
     moe::PackParams pp;

@@ -28,6 +28,48 @@ size_t route_count_smem_bytes(int E);
 // idx_vec: 4, 2 or 1 int32 per load (K % idx_vec == 0, topk_idx aligned to 4*idx_vec bytes).
 cudaError_t launch_route_count(const RouteCountParams& p, int idx_vec, cudaStream_t stream);
 
+// ---- route_local + route_finalize: the same results from many blocks --------
+constexpr int kSplitThreads = 256;    // tokens per sub-chunk (one per thread)
+constexpr int kMaxSplitBlocks = 128;  // chunks (blocks) at most; workspace holds kMaxSplitBlocks*E counts
+struct RouteSplitParams {
+  const int32_t* topk_idx;  // [T, K]
+  int32_t T, K, E, N;
+  int32_t chunk;            // tokens per block, a multiple of kSplitThreads
+  int32_t* expert_counts;   // [E]
+  int32_t* expert_offsets;  // [E+1]
+  int32_t* src_offsets;     // [E*N]
+  int32_t* rank_offsets;    // [N+1]
+  int32_t* slot_row;        // [T*K]
+  int32_t* row_src;         // [T*K]
+  int32_t* error_word;      // [1]
+  int32_t* hist;            // [blocks*E] per-chunk expert histograms
+  int32_t* block_err;       // [blocks]   per-chunk routing error flags
+};
+size_t route_local_smem_bytes(int E);
+int route_split_chunk(int T);
+cudaError_t launch_route_split(const RouteSplitParams& p, int idx_vec, cudaStream_t stream);
+
+// ---- route_cluster: the same results from one cluster of <= 16 CTAs ---------
+constexpr int kClusterThreads = 1024;
+constexpr int kMaxClusterCtas = 16;
+struct RouteClusterParams {
+  const int32_t* topk_idx;  // [T, K]
+  int32_t T, K, E, N;
+  int32_t chunk;            // tokens per CTA (multiple of 32)
+  int32_t warps;            // warps of tokens per sub-chunk (<= 32)
+  int32_t* expert_counts;   // [E]
+  int32_t* expert_offsets;  // [E+1]
+  int32_t* src_offsets;     // [E*N]
+  int32_t* rank_offsets;    // [N+1]
+  int32_t* slot_row;        // [T*K]
+  int32_t* row_src;         // [T*K]
+  int32_t* error_word;      // [1]
+};
+size_t route_cluster_smem_bytes(int E, int warps);
+void route_cluster_shape(int T, int E, int max_cluster, int* cluster, int* chunk, int* warps);
+bool route_cluster_supported(const RouteClusterParams& p, int idx_vec, int cluster);
+cudaError_t launch_route_cluster(const RouteClusterParams& p, int idx_vec, int cluster, cudaStream_t stream);
+
 // ---- dispatch_pack: expert_x[slot_row[t,k]] = x[t] --------------------------
 struct PackParams {
   const uint8_t* x;         // [T, row_bytes]

@@ -21,12 +21,14 @@ LIB_PATH = os.path.join(PKG, "libmoe.so")
 MOE_OK, MOE_EINVAL, MOE_ESTATE, MOE_EROUTE, MOE_ECUDA, MOE_EBOUND, MOE_ETIMEDOUT = range(7)
 MOE_MAX_TOP_K = 16
 MOE_MAX_EXPERTS = 1024
-MOE_OPT_PACK_VARIANT, MOE_OPT_PACK_STAGES, MOE_OPT_PACK_PIECE_BYTES, MOE_OPT_PACK_CTAS_PER_SM, MOE_OPT_PDL = 1, 2, 3, 4, 5
+(MOE_OPT_PACK_VARIANT, MOE_OPT_PACK_STAGES, MOE_OPT_PACK_PIECE_BYTES, MOE_OPT_PACK_CTAS_PER_SM, MOE_OPT_PDL,
+ MOE_OPT_ROUTE_VARIANT, MOE_OPT_ROUTE_CLUSTER_CTAS) = 1, 2, 3, 4, 5, 6, 7
+ROUTE_AUTO, ROUTE_SINGLE, ROUTE_SPLIT, ROUTE_CLUSTER = 0, 1, 2, 3
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.
 EXPORTS = ("moe_validate_config", "moe_workspace_bytes", "moe_recv_bound_rows", "moe_ctx_create",
-           "moe_ctx_destroy", "moe_ctx_set_option", "moe_dispatch_send", "moe_dispatch_recv",
+           "moe_ctx_destroy", "moe_ctx_set_option", "moe_ctx_get_option", "moe_dispatch_send", "moe_dispatch_recv",
            "moe_combine_send", "moe_combine_recv", "moe_get_error", "moe_strerror",
            "moe_dispatch_send_noalloc")
 
@@ -70,6 +72,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_ctx_create": ([C, P, ctypes.c_size_t, ctypes.POINTER(P)], I),
         "moe_ctx_destroy": ([P], I),
         "moe_ctx_set_option": ([P, I, I64], I),
+        "moe_ctx_get_option": ([P, I, ctypes.POINTER(ctypes.c_int64)], I),
         "moe_dispatch_send": ([P, P, P, P, I64, P], I),
         "moe_dispatch_recv": ([P, ctypes.POINTER(moe_dispatch_layout), P], I),
         "moe_combine_send": ([P, P, I64, P], I),
@@ -144,6 +147,12 @@ def moe_ctx_set_option(ctx: int, option: int, value: int) -> None:
     _check(load_library().moe_ctx_set_option(ctx, option, value), "moe_ctx_set_option")
 
 
+def moe_ctx_get_option(ctx: int, option: int) -> int:
+    v = ctypes.c_int64(0)
+    _check(load_library().moe_ctx_get_option(ctx, option, ctypes.byref(v)), "moe_ctx_get_option")
+    return int(v.value)
+
+
 def moe_dispatch_send(ctx: int, x: Any, topk_idx: Any, expert_x: Any, expert_x_rows: int, stream: Any = None) -> None:
     _check(load_library().moe_dispatch_send(ctx, _ptr(x), _ptr(topk_idx), _ptr(expert_x), expert_x_rows,
                                             _stream(stream)), "moe_dispatch_send")
@@ -215,7 +224,7 @@ class MoELayer:
             self.ctx = moe_ctx_create(self.cfg, self.workspace, self.workspace.numel())
         names = {"pack_variant": MOE_OPT_PACK_VARIANT, "pack_stages": MOE_OPT_PACK_STAGES,
                  "pack_piece_bytes": MOE_OPT_PACK_PIECE_BYTES, "pack_ctas_per_sm": MOE_OPT_PACK_CTAS_PER_SM,
-                 "pdl": MOE_OPT_PDL}
+                 "pdl": MOE_OPT_PDL, "route_variant": MOE_OPT_ROUTE_VARIANT}
         for k, v in options.items():
             moe_ctx_set_option(self.ctx, names[k], int(v))
 
@@ -232,6 +241,14 @@ class MoELayer:
 
     def set_option(self, option: int, value: int) -> None:
         moe_ctx_set_option(self.ctx, option, value)
+
+    def get_option(self, option: int) -> int:
+        return moe_ctx_get_option(self.ctx, option)
+
+    def kernels_per_layer(self) -> int:
+        """Kernel launches of one dispatch+combine layer (T > 0)."""
+        route = self.get_option(MOE_OPT_ROUTE_VARIANT)
+        return (2 if route == ROUTE_SPLIT else 1) + 2
 
     def dispatch_send(self, x, topk_idx, expert_x, stream: Any = None) -> None:
         moe_dispatch_send(self.ctx, x, topk_idx, expert_x, expert_x.shape[0], stream)

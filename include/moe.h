@@ -109,11 +109,13 @@ int moe_ctx_create(const moe_config* cfg, void* workspace, size_t workspace_byte
 int moe_ctx_destroy(moe_ctx* ctx);
 
 /* Dispatch, send half ("Enabling trillion-parameter models on AWS EFA",
- * Dispatch and combine: count tokens per expert with shared-memory atomics in
- * one block, take the cumulative sum of the counts, pack the tokens at those
- * offsets).  Enqueues route_count (one block: counts, exclusive scan,
- * stable slot ranks, routing error check) and dispatch_pack (copies each
- * token row x[t] to expert_x[slot_row[t,k]] for every k).
+ * Dispatch and combine: count tokens per expert with shared-memory atomics,
+ * take the cumulative sum of the counts, pack the tokens at those offsets).
+ * Enqueues the routing kernels (counts, exclusive scan, stable slot ranks,
+ * routing error check: by default route_cluster, one thread-block cluster of
+ * up to 16 CTAs that exchange per-chunk counts through distributed shared
+ * memory; see MOE_OPT_ROUTE_VARIANT) and dispatch_pack (copies each token row
+ * x[t] to expert_x[slot_row[t,k]] for every k).
  *   x         device bf16 [T, H], read only
  *   topk_idx  device int32 [T, K], read only, 4-byte aligned
  *   expert_x  device bf16 [expert_x_rows, H]; rows [0, T*K) are written,
@@ -157,13 +159,27 @@ int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void* stream)
  *                             16, 0 = automatic (whole row up to 16 KiB)
  *   MOE_OPT_PACK_CTAS_PER_SM  0 = as many as fit, else 1..32
  *   MOE_OPT_PDL               1 = launch pack/combine with programmatic
- *                             dependent launch (default), 0 = plain launches */
+ *                             dependent launch (default), 0 = plain launches
+ *   MOE_OPT_ROUTE_VARIANT     routing kernels: 0 = automatic (route_cluster
+ *                             when the device can schedule its cluster, else
+ *                             route_local + route_finalize), 1 = the
+ *                             single-block route_count, 2 = route_local +
+ *                             route_finalize, 3 = route_cluster (MOE_EINVAL
+ *                             if the device cannot schedule it) */
 #define MOE_OPT_PACK_VARIANT 1
 #define MOE_OPT_PACK_STAGES 2
 #define MOE_OPT_PACK_PIECE_BYTES 3
 #define MOE_OPT_PACK_CTAS_PER_SM 4
 #define MOE_OPT_PDL 5
+#define MOE_OPT_ROUTE_VARIANT 6
 int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
+
+/* Reads back a launch option.  For MOE_OPT_ROUTE_VARIANT set to 0
+ * (automatic) it reports the path dispatch will take (2 or 3);
+ * MOE_OPT_ROUTE_CLUSTER_CTAS reports the route_cluster cluster size chosen
+ * for this configuration (0 if the device cannot schedule it). */
+#define MOE_OPT_ROUTE_CLUSTER_CTAS 7
+int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
 /* ---- Dispatch without any device allocation ------------------------------
  * The pages have no counterpart to this call; it exists for callers that

@@ -150,6 +150,10 @@ PACK_OPTIONS = [
     dict(pack_variant=0, pdl=0),
     dict(pack_variant=1),
     dict(pack_variant=1, pack_piece_bytes=1024, pdl=0),
+    dict(route_variant=1),
+    dict(route_variant=1, pdl=0, pack_variant=1),
+    dict(route_variant=2),
+    dict(route_variant=2, pdl=0),
 ]
 
 
@@ -175,16 +179,19 @@ EDGE = [
     (64, 8200, 2, 8, 2, "uniform_random"),      # row > 16 KiB: split into pieces
     (4096, 2056, 6, 96, 16, "uniform_random"),  # odd-ish row bytes (4112)
     (8192, 64, 8, 64, 8, "rank0_only"),         # everything to rank 0
+    (40960, 16, 2, 64, 8, "uniform_random"),    # > 128 chunks of 256: 512-token chunks in the split routing
+    (33024, 8, 1, 8, 4, "uniform_random"),      # chunk of 512 with a ragged last chunk
 ]
 
 
+@pytest.mark.parametrize("route_variant", [0, 1, 2], ids=["auto", "single", "split"])
 @pytest.mark.parametrize("shape", EDGE, ids=["x".join(map(str, s[:5])) for s in EDGE])
-def test_edge_shapes(moe, oracle_mod, shape):
+def test_edge_shapes(moe, oracle_mod, shape, route_variant):
     T, H, K, E, N, router = shape
     w = gen.custom("edge", T=T, H=H, K=K, E=E, N=N, router=router, seed_index=11)
     li = gen.make_inputs(w)
     d, out_ref = oracle_of(oracle_mod, w, li)
-    res = run_gpu(moe, w, li, extra_rows=5)
+    res = run_gpu(moe, w, li, extra_rows=5, route_variant=route_variant)
     assert_parity(res, d, out_ref, w, extra_rows=5)
 
 
@@ -214,8 +221,9 @@ def test_non_default_stream_and_reuse(moe, oracle_mod):
         assert_parity(res, d, out_ref, w)
 
 
+@pytest.mark.parametrize("route_variant", [0, 1, 2], ids=["auto", "single", "split"])
 @pytest.mark.parametrize("bad", ["out_of_range", "negative", "repeated"])
-def test_routing_errors_write_nothing(moe, bad):
+def test_routing_errors_write_nothing(moe, bad, route_variant):
     w = gen.custom("bad", T=300, H=64, K=4, E=16, N=4, seed_index=3)
     li = gen.make_inputs(w)
     idx = li.topk_idx.copy()
@@ -226,7 +234,7 @@ def test_routing_errors_write_nothing(moe, bad):
     else:
         idx[299, 3] = idx[299, 1]
     li2 = gen.LayerInputs(w, li.x, idx, li.topk_w, li.y)
-    res = run_gpu(moe, w, li2)
+    res = run_gpu(moe, w, li2, route_variant=route_variant)
     assert res["status"] == moe.MOE_EROUTE
     assert res["error_word"][0] == moe.MOE_EROUTE
     assert res["guards_ok"]
@@ -241,6 +249,16 @@ def test_routing_errors_write_nothing(moe, bad):
     out = torch.empty((T, H), dtype=torch.int16, device="cuda")
     layer.layer(x, _dev(li.topk_idx), _dev(li.topk_w), ex, _dev(li.y.view(np.int16)), out)
     assert layer.get_error() == moe.MOE_OK
+
+
+def test_cluster_routing_is_available_on_this_device(moe):
+    """The default routing path on a GB300 is the 16-CTA cluster kernel."""
+    layer = moe.MoELayer(4096, 7168, 8, 256, 32)
+    assert layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS) == 16
+    assert layer.get_option(moe.MOE_OPT_ROUTE_VARIANT) == moe.ROUTE_CLUSTER
+    assert layer.kernels_per_layer() == 3
+    layer.set_option(moe.MOE_OPT_ROUTE_VARIANT, moe.ROUTE_SPLIT)
+    assert layer.kernels_per_layer() == 4
 
 
 def test_call_order_and_argument_checks(moe):
