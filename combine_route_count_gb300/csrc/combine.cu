@@ -87,6 +87,196 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) combine_kernel(CombinePa
   ptx::st_v4(p.out + t * row_bytes + c * 16, o);
 }
 
+// ---- bulk variant: a producer warp gathers with the TMA engine ---------------
+//
+// Work unit = (token t, column piece j of the row); CTA b takes a contiguous
+// range of units, so the K rows of one token serve its P consecutive pieces
+// and the next token's slot_row entries are fetched while the current token
+// is in flight.  Stage s holds the K gathered row pieces (K * piece bytes):
+//   producer (warp 0): waits until stage s is free, lane 0 posts the expected
+//     bytes on full[s], lanes k < K each bulk-load row slot_row[t,k]'s piece;
+//   consumers (warps 1..): wait on full[s], each thread reads its 16-byte
+//     column chunk of the K pieces from shared memory in k order, runs the
+//     FMA chain, stores 16 bytes of out[t], and its warp arrives on empty[s].
+// All waits are bounded (2 s); a timeout sets MOE_ETIMEDOUT in the error word.
+
+constexpr int kBulkBarBytes = 256;  // full[8] + empty[8] mbarriers + skip flags
+constexpr int kMaxBulkStages = 8;
+constexpr int kBulkMaxPiece = 4096;                    // 256 consumer threads
+constexpr int kBulkMaxThreads = 32 + kBulkMaxPiece / 16;  // producer warp + consumers
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const unsigned long long start = globaltimer_ns();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - start > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ptx::smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(ptx::smem_addr(p)));
+  return v;
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(CombineParams p, BulkCombineShape sh) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxBulkStages;
+  int32_t* skip = reinterpret_cast<int32_t*>(empty + kMaxBulkStages);
+  uint8_t* stage_buf = smem + kBulkBarBytes;
+  const int S = sh.stages, P = sh.pieces, PB = sh.piece_bytes;
+  const int K = p.K;
+  const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
+  const int64_t stage_bytes = static_cast<int64_t>(K) * PB;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int consumer_warps = (blockDim.x >> 5) - 1;
+
+  // Contiguous unit range of this CTA.
+  const int64_t units = static_cast<int64_t>(p.T) * P;
+  const int64_t q = units / gridDim.x, rem = units % gridDim.x;
+  const int64_t u0 = blockIdx.x * q + (blockIdx.x < rem ? blockIdx.x : rem);
+  const int64_t n = q + (blockIdx.x < rem ? 1 : 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], consumer_warps);
+    }
+    ptx::mbar_fence_init();
+  }
+  __syncthreads();
+  ptx::wait_prerequisites();  // y and slot_row come from earlier kernels
+
+  auto piece_len = [&](int j) -> uint32_t {
+    const int64_t left = row_bytes - static_cast<int64_t>(j) * PB;
+    return static_cast<uint32_t>(left < PB ? left : PB);
+  };
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    int64_t t_cur = -1;
+    int row = -1, next_row = -1;
+    if (n > 0 && lane < K) {
+      const int64_t t0 = u0 / P;
+      next_row = p.slot_row[t0 * K + lane];
+    }
+    bool ok = true;
+    for (int64_t i = 0; i < n; ++i) {
+      const int s = static_cast<int>(i % S);
+      const int64_t u = u0 + i;
+      const int64_t t = u / P;
+      const int j = static_cast<int>(u - t * P);
+      if (t != t_cur) {
+        t_cur = t;
+        row = next_row;
+        // Prefetch the next token's rows while this one is in flight.
+        const int64_t tn = t + 1;
+        if (lane < K && tn * P < u0 + n) next_row = p.slot_row[tn * K + lane];
+      }
+      if (i >= S) {
+        const bool freed = wait_parity(&empty[s], static_cast<uint32_t>(((i / S) - 1) & 1));
+        if (!__all_sync(0xffffffffu, freed)) {
+          ok = false;
+          break;
+        }
+      }
+      const bool bad = __any_sync(0xffffffffu, lane < K && row < 0);
+      const uint32_t bytes = piece_len(j);
+      if (lane == 0) {
+        skip[s] = bad ? 1 : 0;
+        if (bad) {
+          mbar_arrive(&full[s]);  // nothing to load: release the consumers, who skip the unit
+        } else {
+          ptx::mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(K) * bytes);
+        }
+      }
+      __syncwarp();
+      if (!bad && lane < K) {
+        ptx::bulk_g2s(stage_buf + s * stage_bytes + static_cast<int64_t>(lane) * PB,
+                      p.y + static_cast<int64_t>(row) * row_bytes + static_cast<int64_t>(j) * PB, bytes, &full[s]);
+      }
+    }
+    if (!ok && lane == 0) atomicCAS(p.error_word, MOE_OK, MOE_ETIMEDOUT);
+  } else {
+    // ---------------- consumers ----------------
+    const int c = threadIdx.x - 32;  // 16-byte column chunk within the piece
+    int64_t t_cur = -1;
+    float wk[KMAX];
+    for (int64_t i = 0; i < n; ++i) {
+      const int s = static_cast<int>(i % S);
+      const int64_t u = u0 + i;
+      const int64_t t = u / P;
+      const int j = static_cast<int>(u - t * P);
+      if (t != t_cur) {
+        t_cur = t;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+          if (k < K) wk[k] = __ldg(p.w + t * K + k);
+      }
+      const bool arrived = wait_parity(&full[s], static_cast<uint32_t>((i / S) & 1));
+      if (!__all_sync(0xffffffffu, arrived)) {
+        if (lane == 0) atomicCAS(p.error_word, MOE_OK, MOE_ETIMEDOUT);
+        break;
+      }
+      const uint32_t bytes = piece_len(j);
+      if (!skip[s] && static_cast<uint32_t>(c) * 16 < bytes) {
+        const uint8_t* src = stage_buf + s * stage_bytes + static_cast<int64_t>(c) * 16;
+        uint4 v[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+          if (k < K) v[k] = lds128(src + static_cast<int64_t>(k) * PB);
+        float a[8];
+#pragma unroll
+        for (int q2 = 0; q2 < 8; ++q2) a[q2] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+          if (k < K) {
+            fma_word(v[k].x, wk[k], a[0], a[1]);
+            fma_word(v[k].y, wk[k], a[2], a[3]);
+            fma_word(v[k].z, wk[k], a[4], a[5]);
+            fma_word(v[k].w, wk[k], a[6], a[7]);
+          }
+        }
+        uint4 o;
+        o.x = pack_bf16x2(a[0], a[1]);
+        o.y = pack_bf16x2(a[2], a[3]);
+        o.z = pack_bf16x2(a[4], a[5]);
+        o.w = pack_bf16x2(a[6], a[7]);
+        ptx::st_v4(p.out + t * row_bytes + static_cast<int64_t>(j) * PB + static_cast<int64_t>(c) * 16, o);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+}
+
+template <int KMAX>
+cudaError_t launch_bulk_k(const CombineParams& p, const CombineLaunch& l, cudaStream_t stream) {
+  const BulkCombineShape& sh = l.shape;
+  const size_t smem = combine_bulk_smem_bytes(sh, p.K);
+  auto* kern = combine_bulk_kernel<KMAX>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  const int threads = 32 + (sh.piece_bytes / 16 + 31) / 32 * 32;
+  return launch_kernel(kern, dim3(l.grid), dim3(threads), smem, stream, l.pdl, p, sh);
+}
+
 template <int KMAX>
 cudaError_t launch_k(const CombineParams& p, bool pdl, cudaStream_t stream) {
   constexpr int MIN_BLOCKS = KMAX >= 16 ? 2 : (KMAX >= 8 ? 3 : 4);
@@ -100,7 +290,42 @@ cudaError_t launch_k(const CombineParams& p, bool pdl, cudaStream_t stream) {
 
 }  // namespace
 
+size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K) {
+  return kBulkBarBytes + static_cast<size_t>(sh.stages) * K * sh.piece_bytes;
+}
+
+BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem) {
+  BulkCombineShape sh;
+  const int64_t row_bytes = static_cast<int64_t>(H) * 2;
+  if (piece_bytes <= 0) {
+    // Pieces of at most 2 KiB (128 consumer threads), equal up to 16 bytes.
+    const int64_t pieces = (row_bytes + 2048 - 1) / 2048;
+    piece_bytes = static_cast<int>((row_bytes / 16 + pieces - 1) / pieces * 16);
+  }
+  if (piece_bytes > kBulkMaxPiece) piece_bytes = kBulkMaxPiece;
+  if (piece_bytes > row_bytes) piece_bytes = static_cast<int>(row_bytes);
+  sh.piece_bytes = piece_bytes;
+  sh.pieces = static_cast<int>((row_bytes + piece_bytes - 1) / piece_bytes);
+  if (stages <= 0) {
+    // About 100 KiB of stages per CTA: two CTAs per SM.
+    stages = static_cast<int>((100 * 1024) / (static_cast<int64_t>(K) * piece_bytes));
+  }
+  if (stages < 2) stages = 2;
+  if (stages > kMaxBulkStages) stages = kMaxBulkStages;
+  while (stages > 2 && combine_bulk_smem_bytes(BulkCombineShape{stages, sh.piece_bytes, sh.pieces}, K) >
+                           static_cast<size_t>(max_smem))
+    --stages;
+  sh.stages = stages;
+  return sh;
+}
+
 cudaError_t launch_combine(const CombineParams& p, const CombineLaunch& l, cudaStream_t stream) {
+  if (l.variant == kCombineBulk) {
+    if (p.K <= 2) return launch_bulk_k<2>(p, l, stream);
+    if (p.K <= 4) return launch_bulk_k<4>(p, l, stream);
+    if (p.K <= 8) return launch_bulk_k<8>(p, l, stream);
+    return launch_bulk_k<16>(p, l, stream);
+  }
   if (p.K <= 2) return launch_k<2>(p, l.pdl, stream);
   if (p.K <= 4) return launch_k<4>(p, l.pdl, stream);
   if (p.K <= 8) return launch_k<8>(p, l.pdl, stream);

@@ -55,7 +55,7 @@ __device__ __forceinline__ void report(int32_t* error_word, int status) {
   atomicCAS(error_word, MOE_OK, status);
 }
 
-__global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stages) {
+__global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stages, int prefetch) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* stage_buf = smem + kBarBytes;
@@ -91,6 +91,15 @@ __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stage
   const int64_t prologue = mine < stages ? mine : stages;
   if (lane == 0)
     for (int64_t i = 0; i < prologue; ++i) issue_load(i);
+  if (prefetch) {
+    // The later rows of this CTA go to L2 now, while routing still runs.
+    for (int64_t i = prologue + lane; i < mine; i += 32) {
+      const int64_t u = first + i * step;
+      const int64_t t = u / p.pieces;
+      const int j = static_cast<int>(u - t * p.pieces);
+      ptx::bulk_prefetch_l2(p.x + t * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes, piece_bytes(j));
+    }
+  }
 
   ptx::wait_prerequisites();  // slot_row is written by route_count
 
@@ -188,7 +197,7 @@ cudaError_t launch_dispatch_pack(const PackParams& p, const PackLaunch& l, cudaS
   }
   const int stages = l.stages < 2 ? 2 : (l.stages > kMaxStages ? kMaxStages : l.stages);
   return launch_kernel(dispatch_pack_bulk, dim3(l.grid), dim3(32), pack_bulk_smem_bytes(stages, p.piece_bytes),
-                       stream, l.pdl, p, stages);
+                       stream, l.pdl, p, stages, l.prefetch ? 1 : 0);
 }
 
 }  // namespace moe

@@ -89,8 +89,13 @@ struct moe_ctx {
   int pack_stages;
   int pack_piece_bytes;  // 0 = automatic
   int pack_ctas_per_sm;  // 0 = as many as fit
+  int pack_prefetch;     // 1 = prefetch the CTA's later token rows into L2 before routing completes
   int pdl;
   int route_variant;  // MOE_OPT_ROUTE_VARIANT
+  int combine_variant;      // MOE_OPT_COMBINE_VARIANT
+  int combine_stages;       // 0 = automatic
+  int combine_piece_bytes;  // 0 = automatic
+  int combine_ctas_per_sm;  // 0 = as many as fit
   int cluster_ctas;   // route_cluster shape for this configuration (0 = cannot be scheduled)
   int cluster_chunk;
   int cluster_warps;
@@ -162,11 +167,13 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->hist = reinterpret_cast<int32_t*>(c->ws + l.hist);
   c->block_err = reinterpret_cast<int32_t*>(c->ws + l.block_err);
   c->pack_variant = moe::kPackBulk;
-  c->pack_stages = 4;
+  c->pack_stages = 8;
+  c->pack_prefetch = 0;
   c->pack_piece_bytes = 0;
   c->pack_ctas_per_sm = 0;
   c->pdl = 1;
   c->route_variant = 0;
+  c->combine_variant = moe::kCombineBulk;
   // Largest cluster of route_cluster CTAs this device can schedule for this
   // configuration (16, else 8, 4, 2, 1), or none.
   for (int maxc = moe::kMaxClusterCtas; maxc >= 1; maxc /= 2) {
@@ -219,6 +226,26 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       if (value != 0 && value != 1) return MOE_EINVAL;
       ctx->pdl = static_cast<int>(value);
       return MOE_OK;
+    case MOE_OPT_PACK_PREFETCH:
+      if (value != 0 && value != 1) return MOE_EINVAL;
+      ctx->pack_prefetch = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_COMBINE_VARIANT:
+      if (value != moe::kCombineBulk && value != moe::kCombineVector) return MOE_EINVAL;
+      ctx->combine_variant = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_COMBINE_STAGES:
+      if (value != 0 && (value < 2 || value > 8)) return MOE_EINVAL;
+      ctx->combine_stages = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_COMBINE_PIECE_BYTES:
+      if (value < 0 || value % 16 != 0 || value > 16384) return MOE_EINVAL;
+      ctx->combine_piece_bytes = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_COMBINE_CTAS_PER_SM:
+      if (value < 0 || value > 32) return MOE_EINVAL;
+      ctx->combine_ctas_per_sm = static_cast<int>(value);
+      return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       if (value < 0 || value > 3) return MOE_EINVAL;
       if (value == 3 && ctx->cluster_ctas == 0) return MOE_EINVAL;
@@ -247,11 +274,26 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
     case MOE_OPT_PDL:
       *value = ctx->pdl;
       return MOE_OK;
+    case MOE_OPT_PACK_PREFETCH:
+      *value = ctx->pack_prefetch;
+      return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       *value = ctx->route_variant != 0 ? ctx->route_variant : (ctx->cluster_ctas > 0 ? 3 : 2);
       return MOE_OK;
     case MOE_OPT_ROUTE_CLUSTER_CTAS:
       *value = ctx->cluster_ctas;
+      return MOE_OK;
+    case MOE_OPT_COMBINE_VARIANT:
+      *value = ctx->combine_variant;
+      return MOE_OK;
+    case MOE_OPT_COMBINE_STAGES:
+      *value = ctx->combine_stages;
+      return MOE_OK;
+    case MOE_OPT_COMBINE_PIECE_BYTES:
+      *value = ctx->combine_piece_bytes;
+      return MOE_OK;
+    case MOE_OPT_COMBINE_CTAS_PER_SM:
+      *value = ctx->combine_ctas_per_sm;
       return MOE_OK;
     default:
       return MOE_EINVAL;
@@ -260,12 +302,12 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
 
 namespace {
 
-// Bytes per pack unit: the whole row when it is at most 16 KiB, else the
-// row split into equal 16-byte-multiple pieces of at most 16 KiB.
+// Bytes per pack unit: the whole row when it is at most 8 KiB, else the row
+// split into equal 16-byte-multiple pieces of at most 8 KiB.
 int pack_piece_bytes(const moe_ctx* c, int64_t row_bytes) {
   int64_t pb = c->pack_piece_bytes;
   if (pb <= 0) {
-    const int64_t pieces = (row_bytes + 16384 - 1) / 16384;
+    const int64_t pieces = (row_bytes + 8192 - 1) / 8192;
     pb = (row_bytes / 16 + pieces - 1) / pieces * 16;
   }
   if (pb > row_bytes) pb = row_bytes;
@@ -386,6 +428,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     }
     pl.grid = pack_grid(ctx, pp, pl.stages);
     pl.pdl = ctx->pdl != 0;
+    pl.prefetch = ctx->pack_prefetch != 0;
     if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
   }
   ctx->phase = kDispatched;
@@ -438,8 +481,24 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
     cp.T = c.num_tokens;
     cp.K = c.top_k;
     cp.H = c.hidden;
+    cp.error_word = ctx->error_word;
     moe::CombineLaunch cl;
     cl.pdl = ctx->pdl != 0;
+    cl.variant = ctx->combine_variant;
+    cl.grid = 0;
+    if (cl.variant == moe::kCombineBulk) {
+      cl.shape = moe::combine_bulk_shape(c.hidden, c.top_k, ctx->combine_stages, ctx->combine_piece_bytes,
+                                         ctx->max_smem_optin);
+      const size_t smem = moe::combine_bulk_smem_bytes(cl.shape, c.top_k);
+      if (smem > static_cast<size_t>(ctx->max_smem_optin)) return MOE_EINVAL;
+      const int fit = static_cast<int>((228 * 1024) / (smem + 1024));
+      int per_sm = ctx->combine_ctas_per_sm > 0 && ctx->combine_ctas_per_sm < fit ? ctx->combine_ctas_per_sm : fit;
+      if (per_sm < 1) per_sm = 1;
+      const int64_t units = static_cast<int64_t>(c.num_tokens) * cl.shape.pieces;
+      int64_t grid = static_cast<int64_t>(ctx->num_sms) * per_sm;
+      if (grid > units) grid = units;
+      cl.grid = static_cast<int>(grid);
+    }
     if (moe::launch_combine(cp, cl, static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ECUDA;
   }
   ctx->expert_y = nullptr;

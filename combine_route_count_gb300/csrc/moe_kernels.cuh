@@ -87,6 +87,7 @@ struct PackLaunch {
   int grid;       // CTAs
   int stages;     // bulk: shared-memory stages per CTA (2..8)
   bool pdl;       // launch with programmatic stream serialization
+  bool prefetch;  // bulk: prefetch the CTA's later rows into L2 in the prologue
 };
 size_t pack_bulk_smem_bytes(int stages, int piece_bytes);
 cudaError_t prepare_pack(int max_smem_bytes);  // one-time per-device attribute setup
@@ -98,11 +99,23 @@ struct CombineParams {
   const float* w;           // [T, K]
   const int32_t* slot_row;  // [T*K]
   uint8_t* out;             // [T, H] bf16
+  int32_t* error_word;      // [1] bounded waits report MOE_ETIMEDOUT here
   int32_t T, K, H;
 };
-struct CombineLaunch {
-  bool pdl;  // launch with programmatic stream serialization
+enum CombineVariant { kCombineBulk = 0, kCombineVector = 1 };
+struct BulkCombineShape {
+  int stages;       // shared-memory stages per CTA
+  int piece_bytes;  // bytes of a row per unit (multiple of 16)
+  int pieces;       // units per token
 };
+struct CombineLaunch {
+  int variant;             // CombineVariant
+  int grid;                // bulk: CTAs
+  BulkCombineShape shape;  // bulk
+  bool pdl;                // launch with programmatic stream serialization
+};
+size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K);
+BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem);
 cudaError_t launch_combine(const CombineParams& p, const CombineLaunch& l, cudaStream_t stream);
 
 // Launch helper: plain or programmatic-dependent launch with cudaLaunchKernelEx.

@@ -153,6 +153,7 @@ MOE_API int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, cons
   if (grid > units) grid = units;
   pl.grid = static_cast<int>(grid);
   pl.pdl = true;
+  pl.prefetch = false;
   if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
   return MOE_OK;
 }

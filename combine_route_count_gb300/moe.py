@@ -24,6 +24,9 @@ MOE_MAX_EXPERTS = 1024
 (MOE_OPT_PACK_VARIANT, MOE_OPT_PACK_STAGES, MOE_OPT_PACK_PIECE_BYTES, MOE_OPT_PACK_CTAS_PER_SM, MOE_OPT_PDL,
  MOE_OPT_ROUTE_VARIANT, MOE_OPT_ROUTE_CLUSTER_CTAS) = 1, 2, 3, 4, 5, 6, 7
 ROUTE_AUTO, ROUTE_SINGLE, ROUTE_SPLIT, ROUTE_CLUSTER = 0, 1, 2, 3
+MOE_OPT_COMBINE_VARIANT, MOE_OPT_COMBINE_STAGES, MOE_OPT_COMBINE_PIECE_BYTES, MOE_OPT_COMBINE_CTAS_PER_SM = 8, 9, 10, 11
+COMBINE_BULK, COMBINE_VECTOR = 0, 1
+MOE_OPT_PACK_PREFETCH = 12
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.
@@ -224,7 +227,10 @@ class MoELayer:
             self.ctx = moe_ctx_create(self.cfg, self.workspace, self.workspace.numel())
         names = {"pack_variant": MOE_OPT_PACK_VARIANT, "pack_stages": MOE_OPT_PACK_STAGES,
                  "pack_piece_bytes": MOE_OPT_PACK_PIECE_BYTES, "pack_ctas_per_sm": MOE_OPT_PACK_CTAS_PER_SM,
-                 "pdl": MOE_OPT_PDL, "route_variant": MOE_OPT_ROUTE_VARIANT}
+                 "pdl": MOE_OPT_PDL, "route_variant": MOE_OPT_ROUTE_VARIANT,
+                 "combine_variant": MOE_OPT_COMBINE_VARIANT, "combine_stages": MOE_OPT_COMBINE_STAGES,
+                 "combine_piece_bytes": MOE_OPT_COMBINE_PIECE_BYTES,
+                 "combine_ctas_per_sm": MOE_OPT_COMBINE_CTAS_PER_SM, "pack_prefetch": MOE_OPT_PACK_PREFETCH}
         for k, v in options.items():
             moe_ctx_set_option(self.ctx, names[k], int(v))
 

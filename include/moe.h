@@ -154,9 +154,10 @@ int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void* stream)
  * configuration).  Returns MOE_EINVAL for an unknown option or value.
  *   MOE_OPT_PACK_VARIANT      0 = bulk copies through shared memory (TMA
  *                             engine, default), 1 = 16-byte vector loads/stores
- *   MOE_OPT_PACK_STAGES       shared-memory stages per bulk CTA, 2..8 (default 4)
+ *   MOE_OPT_PACK_STAGES       shared-memory stages per bulk CTA, 2..8 (default 8)
  *   MOE_OPT_PACK_PIECE_BYTES  bytes of a row moved per work unit, a multiple of
- *                             16, 0 = automatic (whole row up to 16 KiB)
+ *                             16, 0 = automatic (whole row up to 8 KiB, else
+ *                             equal pieces of at most 8 KiB)
  *   MOE_OPT_PACK_CTAS_PER_SM  0 = as many as fit, else 1..32
  *   MOE_OPT_PDL               1 = launch pack/combine with programmatic
  *                             dependent launch (default), 0 = plain launches
@@ -179,6 +180,20 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  * MOE_OPT_ROUTE_CLUSTER_CTAS reports the route_cluster cluster size chosen
  * for this configuration (0 if the device cannot schedule it). */
 #define MOE_OPT_ROUTE_CLUSTER_CTAS 7
+/*   MOE_OPT_COMBINE_VARIANT     0 = a producer warp gathers the K expert-row
+ *                               pieces with bulk copies into shared-memory
+ *                               stages, consumer warps reduce (default);
+ *                               1 = one thread per 16-byte chunk, direct loads
+ *   MOE_OPT_COMBINE_STAGES      bulk: stages per CTA, 2..8, 0 = automatic
+ *   MOE_OPT_COMBINE_PIECE_BYTES bulk: bytes of a row per unit, 0 = automatic
+ *   MOE_OPT_COMBINE_CTAS_PER_SM bulk: 0 = as many as fit, else 1..32 */
+#define MOE_OPT_COMBINE_VARIANT 8
+#define MOE_OPT_COMBINE_STAGES 9
+#define MOE_OPT_COMBINE_PIECE_BYTES 10
+#define MOE_OPT_COMBINE_CTAS_PER_SM 11
+/*   MOE_OPT_PACK_PREFETCH       bulk pack: 1 = prefetch each CTA's later token
+ *                               rows into L2 while routing runs, 0 = off */
+#define MOE_OPT_PACK_PREFETCH 12
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
 /* ---- Dispatch without any device allocation ------------------------------

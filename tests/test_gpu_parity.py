@@ -154,6 +154,10 @@ PACK_OPTIONS = [
     dict(route_variant=1, pdl=0, pack_variant=1),
     dict(route_variant=2),
     dict(route_variant=2, pdl=0),
+    dict(combine_variant=1),
+    dict(combine_variant=0, combine_stages=2, combine_piece_bytes=1024),
+    dict(combine_variant=0, combine_stages=8, combine_piece_bytes=2048 + 16, combine_ctas_per_sm=1),
+    dict(combine_variant=0, combine_piece_bytes=4096, pdl=0),
 ]
 
 
@@ -184,14 +188,17 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("route_variant", [0, 1, 2], ids=["auto", "single", "split"])
+VARIANTS = [(0, 0), (1, 1), (2, 0)]  # (route_variant, combine_variant)
+
+
+@pytest.mark.parametrize("variants", VARIANTS, ids=["cluster-bulk", "single-vector", "split-bulk"])
 @pytest.mark.parametrize("shape", EDGE, ids=["x".join(map(str, s[:5])) for s in EDGE])
-def test_edge_shapes(moe, oracle_mod, shape, route_variant):
+def test_edge_shapes(moe, oracle_mod, shape, variants):
     T, H, K, E, N, router = shape
     w = gen.custom("edge", T=T, H=H, K=K, E=E, N=N, router=router, seed_index=11)
     li = gen.make_inputs(w)
     d, out_ref = oracle_of(oracle_mod, w, li)
-    res = run_gpu(moe, w, li, extra_rows=5, route_variant=route_variant)
+    res = run_gpu(moe, w, li, extra_rows=5, route_variant=variants[0], combine_variant=variants[1])
     assert_parity(res, d, out_ref, w, extra_rows=5)
 
 
@@ -221,9 +228,9 @@ def test_non_default_stream_and_reuse(moe, oracle_mod):
         assert_parity(res, d, out_ref, w)
 
 
-@pytest.mark.parametrize("route_variant", [0, 1, 2], ids=["auto", "single", "split"])
+@pytest.mark.parametrize("variants", VARIANTS, ids=["cluster-bulk", "single-vector", "split-bulk"])
 @pytest.mark.parametrize("bad", ["out_of_range", "negative", "repeated"])
-def test_routing_errors_write_nothing(moe, bad, route_variant):
+def test_routing_errors_write_nothing(moe, bad, variants):
     w = gen.custom("bad", T=300, H=64, K=4, E=16, N=4, seed_index=3)
     li = gen.make_inputs(w)
     idx = li.topk_idx.copy()
@@ -234,7 +241,7 @@ def test_routing_errors_write_nothing(moe, bad, route_variant):
     else:
         idx[299, 3] = idx[299, 1]
     li2 = gen.LayerInputs(w, li.x, idx, li.topk_w, li.y)
-    res = run_gpu(moe, w, li2, route_variant=route_variant)
+    res = run_gpu(moe, w, li2, route_variant=variants[0], combine_variant=variants[1])
     assert res["status"] == moe.MOE_EROUTE
     assert res["error_word"][0] == moe.MOE_EROUTE
     assert res["guards_ok"]
