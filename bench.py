@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--buffer-sets", type=int, default=2)
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step per buffer set in a CUDA graph and replay it")
     return ap.parse_args()
 
 
@@ -258,6 +260,22 @@ def run_gpu(args):
     if layer.get_error(stream) != moe.MOE_OK:
         raise RuntimeError("device reported an error during warm-up")
 
+    run_steps = None
+    if args.graph:
+        # One replay = one step on each buffer set, in order.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for s_ in sets:
+                step(s_)
+        torch.cuda.synchronize(dev)
+
+        def run_steps(k):
+            with torch.cuda.stream(stream):
+                for _ in range(k // len(sets)):
+                    graph.replay()
+            for i in range(k % len(sets)):
+                step(sets[i])
+
     clocks = ClockSampler(torch.cuda.current_device() if ws == 1 else local).start()
     time.sleep(0.2)
     # Headline: exactly K steps between one pair of events, nothing recorded
@@ -269,8 +287,11 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
     t_start.record(stream)
-    for i in range(args.steps):
-        step(sets[i % len(sets)])
+    if run_steps is not None:
+        run_steps(args.steps)
+    else:
+        for i in range(args.steps):
+            step(sets[i % len(sets)])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -346,7 +367,12 @@ def run_gpu(args):
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": f"inputs > L2: {ab['total'] / 1e6:.0f} MB moved per layer, "
                              f"{args.buffer_sets} rotating buffer sets",
-                       "pack": "bulk (TMA), PDL",
+                       "launch": "CUDA graph replay" if args.graph else "direct C-ABI calls",
+                       "pack": f"bulk (TMA), {layer.get_option(moe.MOE_OPT_PACK_STAGES) or 'auto'} stages, "
+                               f"prefetch={layer.get_option(moe.MOE_OPT_PACK_PREFETCH)}, "
+                               f"hints={layer.get_option(moe.MOE_OPT_CACHE_HINTS)}, PDL",
+                       "combine": "bulk (TMA gather)" if layer.get_option(moe.MOE_OPT_COMBINE_VARIANT) == 0
+                                  else "vector",
                        "routing": {1: "route_count (1 block)", 2: "route_local+route_finalize",
                                    3: f"route_cluster ({layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS)} CTAs)"}[
                            layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)]},

@@ -170,6 +170,8 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
 
   if (warp == 0) {
     // ---------------- producer ----------------
+    const int hints = sh.hints;
+    const uint64_t pol = hints ? ptx::policy_evict_first() : 0;
     int64_t t_cur = -1;
     int row = -1, next_row = -1;
     if (n > 0 && lane < K) {
@@ -208,8 +210,12 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
       }
       __syncwarp();
       if (!bad && lane < K) {
-        ptx::bulk_g2s(stage_buf + s * stage_bytes + static_cast<int64_t>(lane) * PB,
-                      p.y + static_cast<int64_t>(row) * row_bytes + static_cast<int64_t>(j) * PB, bytes, &full[s]);
+        uint8_t* dst = stage_buf + s * stage_bytes + static_cast<int64_t>(lane) * PB;
+        const uint8_t* src = p.y + static_cast<int64_t>(row) * row_bytes + static_cast<int64_t>(j) * PB;
+        if (hints & kHintCombineLoads)
+          ptx::bulk_g2s_hint(dst, src, bytes, &full[s], pol);
+        else
+          ptx::bulk_g2s(dst, src, bytes, &full[s]);
       }
     }
     if (!ok && lane == 0) atomicCAS(p.error_word, MOE_OK, MOE_ETIMEDOUT);
@@ -271,7 +277,7 @@ cudaError_t launch_bulk_k(const CombineParams& p, const CombineLaunch& l, cudaSt
   const BulkCombineShape& sh = l.shape;
   const size_t smem = combine_bulk_smem_bytes(sh, p.K);
   auto* kern = combine_bulk_kernel<KMAX>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t err = set_kernel_limits(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   const int threads = 32 + (sh.piece_bytes / 16 + 31) / 32 * 32;
   return launch_kernel(kern, dim3(l.grid), dim3(threads), smem, stream, l.pdl, p, sh);
@@ -296,6 +302,7 @@ size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K) {
 
 BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem) {
   BulkCombineShape sh;
+  sh.hints = 0;
   const int64_t row_bytes = static_cast<int64_t>(H) * 2;
   if (piece_bytes <= 0) {
     // Pieces of at most 2 KiB (128 consumer threads), equal up to 16 bytes.
@@ -312,7 +319,7 @@ BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, i
   }
   if (stages < 2) stages = 2;
   if (stages > kMaxBulkStages) stages = kMaxBulkStages;
-  while (stages > 2 && combine_bulk_smem_bytes(BulkCombineShape{stages, sh.piece_bytes, sh.pieces}, K) >
+  while (stages > 2 && combine_bulk_smem_bytes(BulkCombineShape{stages, sh.piece_bytes, sh.pieces, 0}, K) >
                            static_cast<size_t>(max_smem))
     --stages;
   sh.stages = stages;

@@ -31,7 +31,7 @@
 namespace moe {
 namespace {
 
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 16;
 constexpr int kBarBytes = 128;  // mbarrier block at the front of shared memory
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -55,7 +55,7 @@ __device__ __forceinline__ void report(int32_t* error_word, int status) {
   atomicCAS(error_word, MOE_OK, status);
 }
 
-__global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stages, int prefetch) {
+__global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stages, int prefetch, int hints) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* stage_buf = smem + kBarBytes;
@@ -75,6 +75,7 @@ __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stage
     const int64_t left = p.row_bytes - static_cast<int64_t>(j) * p.piece_bytes;
     return static_cast<uint32_t>(left < p.piece_bytes ? left : p.piece_bytes);
   };
+  const uint64_t pol = hints ? ptx::policy_evict_first() : 0;
   auto issue_load = [&](int64_t i) {
     const int64_t u = first + i * step;
     const int64_t t = u / p.pieces;
@@ -82,8 +83,12 @@ __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stage
     const uint32_t bytes = piece_bytes(j);
     const int s = static_cast<int>(i % stages);
     ptx::mbar_arrive_expect_tx(&bars[s], bytes);
-    ptx::bulk_g2s(stage_buf + static_cast<size_t>(s) * p.piece_bytes,
-                  p.x + t * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes, bytes, &bars[s]);
+    if (hints & kHintPackLoads)
+      ptx::bulk_g2s_hint(stage_buf + static_cast<size_t>(s) * p.piece_bytes,
+                         p.x + t * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes, bytes, &bars[s], pol);
+    else
+      ptx::bulk_g2s(stage_buf + static_cast<size_t>(s) * p.piece_bytes,
+                    p.x + t * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes, bytes, &bars[s]);
   };
 
   // Token rows are ready before this grid starts: prefetch while the routing
@@ -119,8 +124,12 @@ __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stage
       break;
     }
     if (row >= 0) {
-      ptx::bulk_s2g(p.expert_x + static_cast<int64_t>(row) * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes,
-                    stage_buf + static_cast<size_t>(s) * p.piece_bytes, piece_bytes(j));
+      uint8_t* dst = p.expert_x + static_cast<int64_t>(row) * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes;
+      const uint8_t* src = stage_buf + static_cast<size_t>(s) * p.piece_bytes;
+      if (hints & kHintPackStores)
+        ptx::bulk_s2g_hint(dst, src, piece_bytes(j), pol);
+      else
+        ptx::bulk_s2g(dst, src, piece_bytes(j));
     }
     ptx::bulk_commit();
     // Refill the stage of unit i-1 once every lane's stores of unit i-1
@@ -188,7 +197,7 @@ size_t pack_bulk_smem_bytes(int stages, int piece_bytes) {
 }
 
 cudaError_t prepare_pack(int max_smem_bytes) {
-  return cudaFuncSetAttribute(dispatch_pack_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_bytes);
+  return set_kernel_limits(reinterpret_cast<const void*>(dispatch_pack_bulk), static_cast<size_t>(max_smem_bytes));
 }
 
 cudaError_t launch_dispatch_pack(const PackParams& p, const PackLaunch& l, cudaStream_t stream) {
@@ -197,7 +206,7 @@ cudaError_t launch_dispatch_pack(const PackParams& p, const PackLaunch& l, cudaS
   }
   const int stages = l.stages < 2 ? 2 : (l.stages > kMaxStages ? kMaxStages : l.stages);
   return launch_kernel(dispatch_pack_bulk, dim3(l.grid), dim3(32), pack_bulk_smem_bytes(stages, p.piece_bytes),
-                       stream, l.pdl, p, stages, l.prefetch ? 1 : 0);
+                       stream, l.pdl, p, stages, l.prefetch ? 1 : 0, l.hints);
 }
 
 }  // namespace moe

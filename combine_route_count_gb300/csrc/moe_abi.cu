@@ -15,12 +15,40 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 
 #include "moe.h"
 #include "moe_kernels.cuh"
 
 #define MOE_API extern "C" __attribute__((visibility("default")))
+
+namespace moe {
+
+cudaError_t set_kernel_limits(const void* kernel, size_t bytes, bool nonportable_cluster) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, std::pair<size_t, bool>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  auto& entry = done[{dev, kernel}];
+  if (bytes > entry.first) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (err != cudaSuccess) return err;
+    entry.first = bytes;
+  }
+  if (nonportable_cluster && !entry.second) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err != cudaSuccess) return err;
+    entry.second = true;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace moe
 
 namespace {
 
@@ -90,6 +118,7 @@ struct moe_ctx {
   int pack_piece_bytes;  // 0 = automatic
   int pack_ctas_per_sm;  // 0 = as many as fit
   int pack_prefetch;     // 1 = prefetch the CTA's later token rows into L2 before routing completes
+  int cache_hints;       // MOE_OPT_CACHE_HINTS bit flags
   int pdl;
   int route_variant;  // MOE_OPT_ROUTE_VARIANT
   int combine_variant;      // MOE_OPT_COMBINE_VARIANT
@@ -167,8 +196,9 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->hist = reinterpret_cast<int32_t*>(c->ws + l.hist);
   c->block_err = reinterpret_cast<int32_t*>(c->ws + l.block_err);
   c->pack_variant = moe::kPackBulk;
-  c->pack_stages = 8;
-  c->pack_prefetch = 0;
+  c->pack_stages = 0;  // automatic: about 100 KiB of stages per CTA
+  c->pack_prefetch = 1;
+  c->cache_hints = moe::kHintPackLoads | moe::kHintPackStores | moe::kHintCombineLoads;
   c->pack_piece_bytes = 0;
   c->pack_ctas_per_sm = 0;
   c->pdl = 1;
@@ -211,7 +241,7 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       ctx->pack_variant = static_cast<int>(value);
       return MOE_OK;
     case MOE_OPT_PACK_STAGES:
-      if (value < 2 || value > 8) return MOE_EINVAL;
+      if (value != 0 && (value < 2 || value > 16)) return MOE_EINVAL;
       ctx->pack_stages = static_cast<int>(value);
       return MOE_OK;
     case MOE_OPT_PACK_PIECE_BYTES:
@@ -229,6 +259,10 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
     case MOE_OPT_PACK_PREFETCH:
       if (value != 0 && value != 1) return MOE_EINVAL;
       ctx->pack_prefetch = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_CACHE_HINTS:
+      if (value < 0 || value > 7) return MOE_EINVAL;
+      ctx->cache_hints = static_cast<int>(value);
       return MOE_OK;
     case MOE_OPT_COMBINE_VARIANT:
       if (value != moe::kCombineBulk && value != moe::kCombineVector) return MOE_EINVAL;
@@ -277,6 +311,9 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
     case MOE_OPT_PACK_PREFETCH:
       *value = ctx->pack_prefetch;
       return MOE_OK;
+    case MOE_OPT_CACHE_HINTS:
+      *value = ctx->cache_hints;
+      return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       *value = ctx->route_variant != 0 ? ctx->route_variant : (ctx->cluster_ctas > 0 ? 3 : 2);
       return MOE_OK;
@@ -316,7 +353,7 @@ int pack_piece_bytes(const moe_ctx* c, int64_t row_bytes) {
 
 int pack_grid(const moe_ctx* c, const moe::PackParams& p, int stages) {
   const int64_t units = static_cast<int64_t>(p.T) * p.pieces;
-  int per_sm = c->pack_ctas_per_sm;
+  int per_sm = c->pack_ctas_per_sm > 0 ? c->pack_ctas_per_sm : (c->pack_variant == moe::kPackBulk ? 2 : 0);
   if (c->pack_variant == moe::kPackBulk) {
     const size_t smem = moe::pack_bulk_smem_bytes(stages, p.piece_bytes);
     // 228 KiB of shared memory per SM, 1 KiB of it reserved per resident CTA.
@@ -418,6 +455,12 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     moe::PackLaunch pl;
     pl.variant = ctx->pack_variant;
     pl.stages = ctx->pack_stages;
+    if (pl.stages <= 0) {
+      // About 100 KiB of stages per CTA (two CTAs per SM), 2..16 stages.
+      pl.stages = static_cast<int>((100 * 1024) / pp.piece_bytes);
+      if (pl.stages > 16) pl.stages = 16;
+      if (pl.stages < 2) pl.stages = 2;
+    }
     if (pl.variant == moe::kPackBulk) {
       // Shrink the pipeline if the stages do not fit in one CTA's shared memory.
       while (pl.stages > 2 &&
@@ -429,6 +472,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     pl.grid = pack_grid(ctx, pp, pl.stages);
     pl.pdl = ctx->pdl != 0;
     pl.prefetch = ctx->pack_prefetch != 0;
+    pl.hints = ctx->cache_hints;
     if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
   }
   ctx->phase = kDispatched;
@@ -489,6 +533,7 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
     if (cl.variant == moe::kCombineBulk) {
       cl.shape = moe::combine_bulk_shape(c.hidden, c.top_k, ctx->combine_stages, ctx->combine_piece_bytes,
                                          ctx->max_smem_optin);
+      cl.shape.hints = ctx->cache_hints;
       const size_t smem = moe::combine_bulk_smem_bytes(cl.shape, c.top_k);
       if (smem > static_cast<size_t>(ctx->max_smem_optin)) return MOE_EINVAL;
       const int fit = static_cast<int>((228 * 1024) / (smem + 1024));

@@ -82,12 +82,15 @@ struct PackParams {
   int32_t pieces;           // ceil(row_bytes / piece_bytes)
 };
 enum PackVariant { kPackBulk = 0, kPackVector = 1 };
+// L2 eviction hints on the bulk copies (bit flags, MOE_OPT_CACHE_HINTS).
+enum CacheHints { kHintPackLoads = 1, kHintPackStores = 2, kHintCombineLoads = 4 };
 struct PackLaunch {
   int variant;    // PackVariant
   int grid;       // CTAs
   int stages;     // bulk: shared-memory stages per CTA (2..8)
   bool pdl;       // launch with programmatic stream serialization
   bool prefetch;  // bulk: prefetch the CTA's later rows into L2 in the prologue
+  int hints;      // CacheHints
 };
 size_t pack_bulk_smem_bytes(int stages, int piece_bytes);
 cudaError_t prepare_pack(int max_smem_bytes);  // one-time per-device attribute setup
@@ -107,6 +110,7 @@ struct BulkCombineShape {
   int stages;       // shared-memory stages per CTA
   int piece_bytes;  // bytes of a row per unit (multiple of 16)
   int pieces;       // units per token
+  int hints;        // CacheHints
 };
 struct CombineLaunch {
   int variant;             // CombineVariant
@@ -117,6 +121,12 @@ struct CombineLaunch {
 size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K);
 BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem);
 cudaError_t launch_combine(const CombineParams& p, const CombineLaunch& l, cudaStream_t stream);
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` (and, if
+// asked, allows non-portable cluster sizes) on the current device.  Each
+// (kernel, device) pair pays the runtime call once; later launches only look
+// the pair up.
+cudaError_t set_kernel_limits(const void* kernel, size_t bytes, bool nonportable_cluster = false);
 
 // Launch helper: plain or programmatic-dependent launch with cudaLaunchKernelEx.
 template <typename... KArgs, typename... Args>

@@ -360,12 +360,8 @@ template <int KMAX, int VEC>
 cudaError_t launch_kv(const RouteClusterParams& p, int cluster, cudaStream_t stream, bool query_only, int* ok) {
   auto* kern = route_cluster_kernel<KMAX, VEC>;
   const size_t smem = route_cluster_smem_bytes(p.E, p.warps);
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t err = set_kernel_limits(reinterpret_cast<const void*>(kern), smem, cluster > 8);
   if (err != cudaSuccess) return err;
-  if (cluster > 8) {
-    err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (err != cudaSuccess) return err;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster);
   cfg.blockDim = dim3(32 * p.warps);

@@ -270,7 +270,7 @@ cudaError_t launch_kmax_vec(const RouteCountParams& p, cudaStream_t stream) {
   constexpr int U = KMAX <= 8 ? 4 : 2;
   auto* kern = route_count_kernel<KMAX, VEC, U>;
   const size_t smem = route_count_smem_bytes(p.E);
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t err = set_kernel_limits(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(1), dim3(kThreads), smem, stream, false, p);
 }

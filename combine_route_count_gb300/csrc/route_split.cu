@@ -299,7 +299,7 @@ cudaError_t launch_split(const RouteSplitParams& p, int blocks, cudaStream_t str
   auto* k2 = route_finalize_kernel<KMAX, VEC>;
   const size_t s1 = route_local_smem_bytes(p.E);
   const size_t s2 = sizeof(int32_t) * (3 * static_cast<size_t>(p.E) + kW + 1);
-  cudaError_t err = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s1));
+  cudaError_t err = set_kernel_limits(reinterpret_cast<const void*>(k1), s1);
   if (err != cudaSuccess) return err;
   err = launch_kernel(k1, dim3(blocks), dim3(kThreads), s1, stream, false, p);
   if (err != cudaSuccess) return err;

@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+from collections.abc import Mapping
 from typing import Any, Dict, Optional
 
 PKG = os.path.dirname(os.path.abspath(__file__))
@@ -27,6 +28,7 @@ ROUTE_AUTO, ROUTE_SINGLE, ROUTE_SPLIT, ROUTE_CLUSTER = 0, 1, 2, 3
 MOE_OPT_COMBINE_VARIANT, MOE_OPT_COMBINE_STAGES, MOE_OPT_COMBINE_PIECE_BYTES, MOE_OPT_COMBINE_CTAS_PER_SM = 8, 9, 10, 11
 COMBINE_BULK, COMBINE_VECTOR = 0, 1
 MOE_OPT_PACK_PREFETCH = 12
+MOE_OPT_CACHE_HINTS = 13
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.
@@ -207,6 +209,45 @@ def moe_dispatch_send_noalloc(cfg: moe_config, x: Any, topk_idx: Any, expert_x: 
 
 # ---- convenience: one context with a torch-allocated workspace ---------------
 
+class DispatchLayout(Mapping):
+    """Read-only mapping over a moe_dispatch_layout: expert_counts [E],
+    expert_offsets [E+1], src_offsets [E, N], rank_offsets [N+1],
+    slot_row [T, K], row_src [T*K], error_word [1] (torch int32 views into the
+    workspace), rows and recv_bound_rows (ints)."""
+
+    _KEYS = ("expert_counts", "expert_offsets", "src_offsets", "rank_offsets", "slot_row", "row_src",
+             "error_word", "rows", "recv_bound_rows")
+
+    def __init__(self, layer: "MoELayer", lay: moe_dispatch_layout):
+        self._layer, self._lay, self._cache = layer, lay, {}
+
+    def __getitem__(self, key: str) -> Any:
+        if key not in self._cache:
+            self._cache[key] = self._make(key)
+        return self._cache[key]
+
+    def __iter__(self):
+        return iter(self._KEYS)
+
+    def __len__(self) -> int:
+        return len(self._KEYS)
+
+    def _make(self, key: str) -> Any:
+        import torch
+        lay, L = self._lay, self._layer
+        if key in ("rows", "recv_bound_rows"):
+            return int(getattr(lay, key))
+        if key not in self._KEYS:
+            raise KeyError(key)
+        T, K, E, N = L.T, L.K, L.E, L.N
+        n, shape = {"expert_counts": (E, None), "expert_offsets": (E + 1, None), "src_offsets": (E * N, (E, N)),
+                    "rank_offsets": (N + 1, None), "slot_row": (T * K, (T, K)), "row_src": (T * K, None),
+                    "error_word": (1, None)}[key]
+        off = (int(getattr(lay, key)) - L.workspace.data_ptr()) // 4
+        v = L.workspace.view(torch.int32)[off:off + n]
+        return v.view(*shape) if shape else v
+
+
 class MoELayer:
     """One dispatch+combine context on the current CUDA device.
 
@@ -230,7 +271,8 @@ class MoELayer:
                  "pdl": MOE_OPT_PDL, "route_variant": MOE_OPT_ROUTE_VARIANT,
                  "combine_variant": MOE_OPT_COMBINE_VARIANT, "combine_stages": MOE_OPT_COMBINE_STAGES,
                  "combine_piece_bytes": MOE_OPT_COMBINE_PIECE_BYTES,
-                 "combine_ctas_per_sm": MOE_OPT_COMBINE_CTAS_PER_SM, "pack_prefetch": MOE_OPT_PACK_PREFETCH}
+                 "combine_ctas_per_sm": MOE_OPT_COMBINE_CTAS_PER_SM, "pack_prefetch": MOE_OPT_PACK_PREFETCH,
+                 "cache_hints": MOE_OPT_CACHE_HINTS}
         for k, v in options.items():
             moe_ctx_set_option(self.ctx, names[k], int(v))
 
@@ -259,23 +301,10 @@ class MoELayer:
     def dispatch_send(self, x, topk_idx, expert_x, stream: Any = None) -> None:
         moe_dispatch_send(self.ctx, x, topk_idx, expert_x, expert_x.shape[0], stream)
 
-    def dispatch_recv(self, stream: Any = None) -> Dict[str, Any]:
-        """Views (torch tensors into the workspace) of the dispatch layout."""
-        lay = moe_dispatch_recv(self.ctx, stream)
-        base = self.workspace.data_ptr()
-        i32 = self.workspace.view(__import__("torch").int32)
-
-        def view(ptr: int, n: int):
-            off = (ptr - base) // 4
-            return i32[off:off + n]
-
-        T, K, E, N = self.T, self.K, self.E, self.N
-        return {"expert_counts": view(lay.expert_counts, E), "expert_offsets": view(lay.expert_offsets, E + 1),
-                "src_offsets": view(lay.src_offsets, E * N).view(E, N),
-                "rank_offsets": view(lay.rank_offsets, N + 1),
-                "slot_row": view(lay.slot_row, T * K).view(T, K), "row_src": view(lay.row_src, T * K),
-                "error_word": view(lay.error_word, 1), "rows": int(lay.rows),
-                "recv_bound_rows": int(lay.recv_bound_rows)}
+    def dispatch_recv(self, stream: Any = None) -> "DispatchLayout":
+        """The dispatch layout; its arrays are torch views into the workspace,
+        made on first access (the call itself only crosses the C ABI)."""
+        return DispatchLayout(self, moe_dispatch_recv(self.ctx, stream))
 
     def combine_send(self, expert_y, stream: Any = None) -> None:
         moe_combine_send(self.ctx, expert_y, expert_y.shape[0], stream)
@@ -286,7 +315,7 @@ class MoELayer:
     def get_error(self, stream: Any = None) -> int:
         return moe_get_error(self.ctx, stream)
 
-    def layer(self, x, topk_idx, topk_w, expert_x, expert_y, out, stream: Any = None) -> Dict[str, Any]:
+    def layer(self, x, topk_idx, topk_w, expert_x, expert_y, out, stream: Any = None) -> "DispatchLayout":
         """dispatch_send -> dispatch_recv -> combine_send -> combine_recv."""
         self.dispatch_send(x, topk_idx, expert_x, stream)
         lay = self.dispatch_recv(stream)

@@ -154,11 +154,12 @@ int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void* stream)
  * configuration).  Returns MOE_EINVAL for an unknown option or value.
  *   MOE_OPT_PACK_VARIANT      0 = bulk copies through shared memory (TMA
  *                             engine, default), 1 = 16-byte vector loads/stores
- *   MOE_OPT_PACK_STAGES       shared-memory stages per bulk CTA, 2..8 (default 8)
+ *   MOE_OPT_PACK_STAGES       shared-memory stages per bulk CTA, 2..16, 0 =
+ *                             automatic (about 100 KiB of stages, default)
  *   MOE_OPT_PACK_PIECE_BYTES  bytes of a row moved per work unit, a multiple of
  *                             16, 0 = automatic (whole row up to 8 KiB, else
  *                             equal pieces of at most 8 KiB)
- *   MOE_OPT_PACK_CTAS_PER_SM  0 = as many as fit, else 1..32
+ *   MOE_OPT_PACK_CTAS_PER_SM  0 = automatic (2 for the bulk variant), else 1..32
  *   MOE_OPT_PDL               1 = launch pack/combine with programmatic
  *                             dependent launch (default), 0 = plain launches
  *   MOE_OPT_ROUTE_VARIANT     routing kernels: 0 = automatic (route_cluster
@@ -192,8 +193,12 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
 #define MOE_OPT_COMBINE_PIECE_BYTES 10
 #define MOE_OPT_COMBINE_CTAS_PER_SM 11
 /*   MOE_OPT_PACK_PREFETCH       bulk pack: 1 = prefetch each CTA's later token
- *                               rows into L2 while routing runs, 0 = off */
+ *                               rows into L2 while routing runs (default), 0 = off */
 #define MOE_OPT_PACK_PREFETCH 12
+/*   MOE_OPT_CACHE_HINTS         bit flags, L2 evict-first policy on: 1 = pack
+ *                               loads, 2 = pack stores, 4 = combine loads
+ *                               (default 7: all streamed data) */
+#define MOE_OPT_CACHE_HINTS 13
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
 /* ---- Dispatch without any device allocation ------------------------------

@@ -158,6 +158,9 @@ PACK_OPTIONS = [
     dict(combine_variant=0, combine_stages=2, combine_piece_bytes=1024),
     dict(combine_variant=0, combine_stages=8, combine_piece_bytes=2048 + 16, combine_ctas_per_sm=1),
     dict(combine_variant=0, combine_piece_bytes=4096, pdl=0),
+    dict(cache_hints=0, pack_prefetch=0),
+    dict(cache_hints=5, pack_prefetch=1, pack_stages=16, pack_ctas_per_sm=1),
+    dict(pack_stages=14, pack_ctas_per_sm=2, combine_stages=5),
 ]
 
 
@@ -266,6 +269,33 @@ def test_cluster_routing_is_available_on_this_device(moe):
     assert layer.kernels_per_layer() == 3
     layer.set_option(moe.MOE_OPT_ROUTE_VARIANT, moe.ROUTE_SPLIT)
     assert layer.kernels_per_layer() == 4
+
+
+def test_layer_replays_from_a_cuda_graph(moe, oracle_mod):
+    """The four calls capture into a CUDA graph (no host sync, no allocation)
+    and replays give the same bits as direct calls."""
+    w = gen.custom("graph", T=1024, H=1024, K=8, E=64, N=8, seed_index=9)
+    li = gen.make_inputs(w)
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    x, idx, wt, y = _dev(li.x.view(np.int16)), _dev(li.topk_idx), _dev(li.topk_w), _dev(li.y.view(np.int16))
+    ex = torch.zeros((w.T * w.K, w.H), dtype=torch.int16, device="cuda")
+    out = torch.zeros((w.T, w.H), dtype=torch.int16, device="cuda")
+    layer = moe.MoELayer(w.T, w.H, w.K, w.E, w.N)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        layer.layer(x, idx, wt, ex, y, out, s)  # first call sets kernel attributes outside the capture
+    torch.cuda.synchronize()
+    ex.zero_()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.layer(x, idx, wt, ex, y, out, s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert layer.get_error() == moe.MOE_OK
+    assert np.array_equal(ex.cpu().numpy().view(np.uint16), d.expert_x)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), out_ref)
 
 
 def test_call_order_and_argument_checks(moe):
