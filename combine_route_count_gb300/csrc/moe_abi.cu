@@ -128,6 +128,8 @@ struct moe_ctx {
   int cluster_ctas;   // route_cluster shape for this configuration (0 = cannot be scheduled)
   int cluster_chunk;
   int cluster_warps;
+  int cluster_staged;
+  int cluster_group;
 };
 
 MOE_API int moe_validate_config(const moe_config* c) {
@@ -209,7 +211,6 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   for (int maxc = moe::kMaxClusterCtas; maxc >= 1; maxc /= 2) {
     int ctas = 0, chunk = 0, warps = 0;
     moe::route_cluster_shape(cfg->num_tokens, cfg->num_experts, maxc, &ctas, &chunk, &warps);
-    if (moe::route_cluster_smem_bytes(cfg->num_experts, warps) > static_cast<size_t>(optin)) continue;
     moe::RouteClusterParams q = {};
     q.T = cfg->num_tokens;
     q.K = cfg->top_k;
@@ -217,10 +218,14 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
     q.N = cfg->num_ranks;
     q.chunk = chunk;
     q.warps = warps;
+    moe::route_cluster_plan(&q, ctas, optin);
+    if (moe::route_cluster_smem_bytes(q.E, warps, q.staged ? chunk * q.K : 0) > static_cast<size_t>(optin)) continue;
     if (moe::route_cluster_supported(q, 1, ctas)) {
       c->cluster_ctas = ctas;
       c->cluster_chunk = chunk;
       c->cluster_warps = warps;
+      c->cluster_staged = q.staged;
+      c->cluster_group = q.dsmem_group;
       break;
     }
   }
@@ -413,6 +418,8 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     cp.N = c.num_ranks;
     cp.chunk = ctx->cluster_chunk;
     cp.warps = ctx->cluster_warps;
+    cp.staged = ctx->cluster_staged;
+    cp.dsmem_group = ctx->cluster_group;
     cp.expert_counts = ctx->expert_counts;
     cp.expert_offsets = ctx->expert_offsets;
     cp.src_offsets = ctx->src_offsets;

@@ -57,6 +57,8 @@ struct RouteClusterParams {
   int32_t T, K, E, N;
   int32_t chunk;            // tokens per CTA (multiple of 32)
   int32_t warps;            // warps of tokens per sub-chunk (<= 32)
+  int32_t staged;           // 1: one sub-chunk per CTA, row_src staged in shared memory
+  int32_t dsmem_group;      // threads per expert in the histogram exchange (power of 2, <= 16)
   int32_t* expert_counts;   // [E]
   int32_t* expert_offsets;  // [E+1]
   int32_t* src_offsets;     // [E*N]
@@ -65,7 +67,9 @@ struct RouteClusterParams {
   int32_t* row_src;         // [T*K]
   int32_t* error_word;      // [1]
 };
-size_t route_cluster_smem_bytes(int E, int warps);
+size_t route_cluster_smem_bytes(int E, int warps, int staged_pairs);
+// Fills chunk/warps/staged/dsmem_group of p for a cluster of `cluster` CTAs.
+void route_cluster_plan(RouteClusterParams* p, int cluster, int max_smem);
 void route_cluster_shape(int T, int E, int max_cluster, int* cluster, int* chunk, int* warps);
 bool route_cluster_supported(const RouteClusterParams& p, int idx_vec, int cluster);
 cudaError_t launch_route_cluster(const RouteClusterParams& p, int idx_vec, int cluster, cudaStream_t stream);

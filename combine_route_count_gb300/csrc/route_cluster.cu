@@ -110,11 +110,14 @@ struct Smem {
   int32_t* hist;   // [E] this chunk's per-expert totals (read by the whole cluster)
   int32_t* base;   // [E] first row of this chunk's tokens per expert
   int32_t* off;    // [E] expert offsets
-  int32_t* wsum;   // [32]
+  int32_t* wsum;   // [64] scan scratch (two scans of up to 32 warp sums)
   int32_t* flag;   // [1] routing error in this chunk (read by the whole cluster)
+  int32_t* lofs;   // [E] chunk-local first row of each expert (staged row_src only)
+  int32_t* sval;   // [chunk*K] staged row_src values, grouped by expert
+  int16_t* sexp;   // [chunk*K] expert of each staged value
 };
 
-__device__ inline Smem carve(int32_t* raw, int E, int S) {
+__device__ inline Smem carve(int32_t* raw, int E, int S, int staged_pairs) {
   Smem s;
   s.mask = reinterpret_cast<uint32_t*>(raw);
   s.lbase = raw + E * S;
@@ -122,33 +125,54 @@ __device__ inline Smem carve(int32_t* raw, int E, int S) {
   s.base = s.hist + E;
   s.off = s.base + E;
   s.wsum = s.off + E;
-  s.flag = s.wsum + 32;
+  s.flag = s.wsum + 64;
+  s.lofs = s.flag + 4;
+  s.sval = s.lofs + E;
+  s.sexp = reinterpret_cast<int16_t*>(s.sval + staged_pairs);
   return s;
 }
 
-// Exclusive scan of in[0..E) into out[0..E) by the whole CTA (each thread
-// takes ceil(E / blockDim.x) consecutive entries; warp-shuffle scans of the
-// per-thread and per-warp sums).
-__device__ void cta_exclusive_scan(const int32_t* in, int32_t* out, int E, int32_t* wsum) {
+// Two exclusive scans in one pass: a[] in place, and (if `second`) b[] into
+// b_out[] (b[] itself is left intact: other CTAs may still read it).
+__device__ void cta_exclusive_scan2(int32_t* a, const int32_t* b, int32_t* b_out, int E, int32_t* wsum,
+                                    bool second) {
   const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
   const int per = (E + nt - 1) / nt;
   const int lo = min(E, tid * per), hi = min(E, lo + per);
-  int sum = 0;
-  for (int i = lo; i < hi; ++i) sum += in[i];
-  const int incl = warp_incl_scan(sum, lane);
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int x = lane < nw ? wsum[lane] : 0;
-    const int xi = warp_incl_scan(x, lane);
-    if (lane < nw) wsum[lane] = xi - x;
+  int sa = 0, sb = 0;
+  for (int i = lo; i < hi; ++i) {
+    sa += a[i];
+    if (second) sb += b[i];
+  }
+  const int ia = warp_incl_scan(sa, lane);
+  const int ib = warp_incl_scan(sb, lane);
+  if (lane == 31) {
+    wsum[warp] = ia;
+    wsum[32 + warp] = ib;
   }
   __syncthreads();
-  int run = incl - sum + wsum[warp];
+  if (warp == 0) {
+    const int xa = lane < nw ? wsum[lane] : 0;
+    const int xb = lane < nw ? wsum[32 + lane] : 0;
+    const int ya = warp_incl_scan(xa, lane);
+    const int yb = warp_incl_scan(xb, lane);
+    __syncwarp();
+    if (lane < nw) {
+      wsum[lane] = ya - xa;
+      wsum[32 + lane] = yb - xb;
+    }
+  }
+  __syncthreads();
+  int ra = ia - sa + wsum[warp];
+  int rb = ib - sb + wsum[32 + warp];
   for (int i = lo; i < hi; ++i) {
-    const int v = in[i];
-    out[i] = run;
-    run += v;
+    const int va = a[i];
+    a[i] = ra;
+    ra += va;
+    if (second) {
+      b_out[i] = rb;
+      rb += b[i];
+    }
   }
   __syncthreads();
 }
@@ -164,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) route_cluster_kernel(RouteCluster
   const int c0 = min(T, static_cast<int>(rank) * p.chunk);
   const int c1 = min(T, c0 + p.chunk);
   const int Tr = T / N;
-  Smem sm = carve(smem_raw, E, S);
+  Smem sm = carve(smem_raw, E, S, p.staged ? p.chunk * K : 0);
 
   // Inputs may come from the previous kernel in the stream: wait for it,
   // then let the pack kernel start fetching token rows.
@@ -203,14 +227,27 @@ __global__ void __launch_bounds__(kThreads, 1) route_cluster_kernel(RouteCluster
       }
     }
     __syncthreads();
-    // Per expert (one per thread): chunk-local base of each warp word.
-    for (int ex = tid; ex < E; ex += SUB) {
-      int run = sm.hist[ex];
-      for (int w = 0; w < W; ++w) {
-        sm.lbase[ex * S + w] = run;
-        run += __popc(sm.mask[ex * S + w]);
+    // Per expert: chunk-local base of each warp word.  Few words: one thread
+    // per expert walks them; many: one warp per expert, shuffle scan.
+    if (W <= 8) {
+      for (int ex = tid; ex < E; ex += SUB) {
+        int run = sm.hist[ex];
+        for (int w = 0; w < W; ++w) {
+          sm.lbase[ex * S + w] = run;
+          run += __popc(sm.mask[ex * S + w]);
+        }
+        sm.hist[ex] = run;
       }
-      sm.hist[ex] = run;
+    } else {
+      for (int ex = warp; ex < E; ex += W) {
+        const int v = lane < W ? __popc(sm.mask[ex * S + lane]) : 0;
+        const int incl = warp_incl_scan(v, lane);
+        const int carry = sm.hist[ex];
+        if (lane < W) sm.lbase[ex * S + lane] = carry + incl - v;
+        const int tot = __shfl_sync(0xffffffffu, incl, 31);
+        __syncwarp();
+        if (lane == 0) sm.hist[ex] = carry + tot;
+      }
     }
     __syncthreads();
     if (mine) {
@@ -230,12 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1) route_cluster_kernel(RouteCluster
       if (Tr > 0) {
         const int s_lo = (s0 + Tr - 1) / Tr;
         const int s_hi = min(N, (s0 + SUB + Tr - 1) / Tr);
-        for (int s = s_lo; s < s_hi; ++s) {
-          const int pos = s * Tr - s0;
-          const uint32_t below = (1u << (pos & 31)) - 1u;
-          for (int ex = tid; ex < E; ex += SUB) {
+        for (int ex = tid; ex < E; ex += SUB) {
+          for (int s = s_lo; s < s_hi; ++s) {
+            const int pos = s * Tr - s0;
             const int i = ex * S + (pos >> 5);
-            p.src_offsets[static_cast<int64_t>(ex) * N + s] = sm.lbase[i] + __popc(sm.mask[i] & below);
+            p.src_offsets[static_cast<int64_t>(ex) * N + s] =
+                sm.lbase[i] + __popc(sm.mask[i] & ((1u << (pos & 31)) - 1u));
           }
         }
       }
@@ -246,23 +283,38 @@ __global__ void __launch_bounds__(kThreads, 1) route_cluster_kernel(RouteCluster
 
   // ---- exchange the chunk histograms through distributed shared memory ----
   cluster_sync();
-  uint32_t remote_hist[kMaxClusterCtas];
-#pragma unroll
-  for (int q = 0; q < kMaxClusterCtas; ++q) remote_hist[q] = q < C ? dsmem_addr(sm.hist, q) : 0u;
   bool any_bad = false;
   if (tid < C) any_bad = ld_dsmem(dsmem_addr(sm.flag, tid)) != 0;
-  for (int ex = tid; ex < E; ex += SUB) {
-    int h[kMaxClusterCtas];
+  {
+    // G threads per expert (G a power of two, G | 32, G * E <= threads)
+    // split the C loads.
+    const int G = p.dsmem_group;
+    const int gshift = __ffs(G) - 1;
+    const int sub = tid & (G - 1);
+    const int rounds = (E * G + SUB - 1) / SUB;
+    for (int rd = 0; rd < rounds; ++rd) {
+      const int ex = (rd * SUB + tid) >> gshift;
+      int tot = 0, before = 0;
+      if (ex < E) {
+        int h[kMaxClusterCtas];
 #pragma unroll
-    for (int q = 0; q < kMaxClusterCtas; ++q) h[q] = q < C ? ld_dsmem(remote_hist[q] + 4u * ex) : 0;
-    int tot = 0, before = 0;
+        for (int q = 0; q < kMaxClusterCtas; ++q)
+          h[q] = (q < C && (q & (G - 1)) == sub) ? ld_dsmem(dsmem_addr(sm.hist + ex, q)) : 0;
 #pragma unroll
-    for (int q = 0; q < kMaxClusterCtas; ++q) {
-      tot += h[q];
-      before += q < static_cast<int>(rank) ? h[q] : 0;
+        for (int q = 0; q < kMaxClusterCtas; ++q) {
+          tot += h[q];
+          before += q < static_cast<int>(rank) ? h[q] : 0;
+        }
+      }
+      for (int o = 1; o < G; o <<= 1) {
+        tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        before += __shfl_xor_sync(0xffffffffu, before, o);
+      }
+      if (ex < E && sub == 0) {
+        sm.off[ex] = tot;  // totals for now; scanned below
+        sm.base[ex] = before;
+      }
     }
-    sm.off[ex] = tot;  // totals for now; scanned below
-    sm.base[ex] = before;
   }
   any_bad = __syncthreads_or(any_bad);
   // Done reading the other CTAs' shared memory: signal it now, wait for the
@@ -287,7 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1) route_cluster_kernel(RouteCluster
 
   if (rank == 0)
     for (int ex = tid; ex < E; ex += SUB) p.expert_counts[ex] = sm.off[ex];
-  cta_exclusive_scan(sm.off, sm.off, E, sm.wsum);  // in place: each thread reads its entries first
+  // In place: expert offsets from the totals and, for staging, the
+  // chunk-local offsets from this chunk's histogram, in one pass.
+  cta_exclusive_scan2(sm.off, sm.hist, sm.lofs, E, sm.wsum, p.staged != 0);
   for (int ex = tid; ex < E; ex += SUB) sm.base[ex] += sm.off[ex];
   __syncthreads();
 
@@ -306,7 +360,30 @@ __global__ void __launch_bounds__(kThreads, 1) route_cluster_kernel(RouteCluster
     }
     store_row<KMAX, VEC>(p.slot_row + static_cast<int64_t>(t) * K, K, rr);
   }
-  if (last_s0 < c1 && last_s0 + tid < c1) {
+  if (p.staged) {
+    // One sub-chunk: r[] are chunk-local ranks.  Stage row_src grouped by
+    // expert in shared memory, then write each expert's run of rows with
+    // consecutive threads (coalesced) instead of one scattered store per pair.
+    if (last_s0 < c1 && last_s0 + tid < c1) {
+      const int t = last_s0 + tid;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (k < K) {
+          const int pos = sm.lofs[e[k]] + r[k];
+          sm.sval[pos] = t * K + k;
+          sm.sexp[pos] = static_cast<int16_t>(e[k]);
+          r[k] += sm.base[e[k]];
+        }
+      }
+      store_row<KMAX, VEC>(p.slot_row + static_cast<int64_t>(t) * K, K, r);
+    }
+    __syncthreads();
+    const int pairs = (c1 - c0) * K;
+    for (int i = tid; i < pairs; i += SUB) {
+      const int ex = sm.sexp[i];
+      p.row_src[sm.base[ex] + (i - sm.lofs[ex])] = sm.sval[i];
+    }
+  } else if (last_s0 < c1 && last_s0 + tid < c1) {
     const int t = last_s0 + tid;
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) {
@@ -321,17 +398,18 @@ __global__ void __launch_bounds__(kThreads, 1) route_cluster_kernel(RouteCluster
   if (Tr > 0) {
     const int s_lo = (c0 + Tr - 1) / Tr;
     const int s_hi = min(N, (c1 + Tr - 1) / Tr);
-    for (int s = s_lo; s < s_hi; ++s) {
-      const int b = s * Tr;
-      if (b >= last_s0) {  // masks of the last sub-chunk are still in shared memory
-        const int pos = b - last_s0;
-        const uint32_t below = (1u << (pos & 31)) - 1u;
-        for (int ex = tid; ex < E; ex += SUB) {
+    for (int ex = tid; ex < E; ex += SUB) {
+      const int bx = sm.base[ex];
+      for (int s = s_lo; s < s_hi; ++s) {
+        const int b = s * Tr;
+        int32_t* dst = p.src_offsets + static_cast<int64_t>(ex) * N + s;
+        if (b >= last_s0) {  // masks of the last sub-chunk are still in shared memory
+          const int pos = b - last_s0;
           const int i = ex * S + (pos >> 5);
-          p.src_offsets[static_cast<int64_t>(ex) * N + s] = sm.base[ex] + sm.lbase[i] + __popc(sm.mask[i] & below);
+          *dst = bx + sm.lbase[i] + __popc(sm.mask[i] & ((1u << (pos & 31)) - 1u));
+        } else {
+          *dst += bx;
         }
-      } else {
-        for (int ex = tid; ex < E; ex += SUB) p.src_offsets[static_cast<int64_t>(ex) * N + s] += sm.base[ex];
       }
     }
   } else if (rank == 0) {
@@ -359,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) route_cluster_kernel(RouteCluster
 template <int KMAX, int VEC>
 cudaError_t launch_kv(const RouteClusterParams& p, int cluster, cudaStream_t stream, bool query_only, int* ok) {
   auto* kern = route_cluster_kernel<KMAX, VEC>;
-  const size_t smem = route_cluster_smem_bytes(p.E, p.warps);
+  const size_t smem = route_cluster_smem_bytes(p.E, p.warps, p.staged ? p.chunk * p.K : 0);
   cudaError_t err = set_kernel_limits(reinterpret_cast<const void*>(kern), smem, cluster > 8);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -404,9 +482,10 @@ cudaError_t dispatch_kv(const RouteClusterParams& p, int idx_vec, int cluster, c
 
 }  // namespace
 
-size_t route_cluster_smem_bytes(int E, int warps) {
+size_t route_cluster_smem_bytes(int E, int warps, int staged_pairs) {
   const size_t S = warps + 1;
-  return sizeof(int32_t) * (2 * static_cast<size_t>(E) * S + 3 * static_cast<size_t>(E) + 32 + 4);
+  return sizeof(int32_t) * (2 * static_cast<size_t>(E) * S + 4 * static_cast<size_t>(E) + 64 + 4) +
+         static_cast<size_t>(staged_pairs) * (sizeof(int32_t) + sizeof(int16_t));
 }
 
 void route_cluster_shape(int T, int E, int max_cluster, int* cluster, int* chunk, int* warps) {
@@ -427,6 +506,18 @@ void route_cluster_shape(int T, int E, int max_cluster, int* cluster, int* chunk
   *warps = w;
 }
 
+void route_cluster_plan(RouteClusterParams* p, int cluster, int max_smem) {
+  const int threads = 32 * p->warps;
+  // Stage row_src when each CTA's chunk is a single sub-chunk and it fits.
+  p->staged = 0;
+  if (p->chunk <= threads &&
+      route_cluster_smem_bytes(p->E, p->warps, p->chunk * p->K) <= static_cast<size_t>(max_smem))
+    p->staged = 1;
+  int g = 1;
+  while (g * 2 <= kMaxClusterCtas && g * 2 <= cluster && g * 2 * p->E <= threads) g *= 2;
+  p->dsmem_group = g;
+}
+
 bool route_cluster_supported(const RouteClusterParams& p, int idx_vec, int cluster) {
   int ok = 0;
   if (dispatch_kv(p, idx_vec, cluster, nullptr, true, &ok) != cudaSuccess) {
@@ -437,6 +528,9 @@ bool route_cluster_supported(const RouteClusterParams& p, int idx_vec, int clust
 }
 
 cudaError_t launch_route_cluster(const RouteClusterParams& p, int idx_vec, int cluster, cudaStream_t stream) {
+  // Wider index loads need K to be a multiple of the width (the caller also
+  // checks the pointer's alignment).
+  if (idx_vec != 1 && p.K % idx_vec != 0) idx_vec = 1;
   int ok = 0;
   return dispatch_kv(p, idx_vec, cluster, stream, false, &ok);
 }

@@ -283,6 +283,9 @@ size_t route_count_smem_bytes(int E) {
 }
 
 cudaError_t launch_route_count(const RouteCountParams& p, int idx_vec, cudaStream_t stream) {
+  // Wider index loads need K to be a multiple of the width (the caller also
+  // checks the pointer's alignment).
+  if (idx_vec != 1 && p.K % idx_vec != 0) idx_vec = 1;
   if (p.K <= 8) {
     if (idx_vec == 4) return launch_kmax_vec<8, 4>(p, stream);
     if (idx_vec == 2) return launch_kmax_vec<8, 2>(p, stream);

@@ -320,6 +320,9 @@ int route_split_chunk(int T) {
 }
 
 cudaError_t launch_route_split(const RouteSplitParams& p, int idx_vec, cudaStream_t stream) {
+  // Wider index loads need K to be a multiple of the width (the caller also
+  // checks the pointer's alignment).
+  if (idx_vec != 1 && p.K % idx_vec != 0) idx_vec = 1;
   const int blocks = p.T > 0 ? (p.T + p.chunk - 1) / p.chunk : 1;
   if (p.K <= 8) {
     if (idx_vec == 4) return launch_split<8, 4>(p, blocks, stream);
