@@ -51,11 +51,27 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Waits until at most `depth` of this thread's bulk store groups still read
+// shared memory (depth 0..7; wait_group takes an immediate).
+__device__ __forceinline__ void wait_reads_at_most(int depth) {
+  switch (depth) {
+    case 0: ptx::bulk_wait_read<0>(); break;
+    case 1: ptx::bulk_wait_read<1>(); break;
+    case 2: ptx::bulk_wait_read<2>(); break;
+    case 3: ptx::bulk_wait_read<3>(); break;
+    case 4: ptx::bulk_wait_read<4>(); break;
+    case 5: ptx::bulk_wait_read<5>(); break;
+    case 6: ptx::bulk_wait_read<6>(); break;
+    default: ptx::bulk_wait_read<7>(); break;
+  }
+}
+
 __device__ __forceinline__ void report(int32_t* error_word, int status) {
   atomicCAS(error_word, MOE_OK, status);
 }
 
-__global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stages, int prefetch, int hints) {
+__global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stages, int prefetch, int hints,
+                                                          int depth) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* stage_buf = smem + kBarBytes;
@@ -132,22 +148,23 @@ __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stage
         ptx::bulk_s2g(dst, src, piece_bytes(j));
     }
     ptx::bulk_commit();
-    // Refill the stage of unit i-1 once every lane's stores of unit i-1
-    // have read it (the stores of unit i stay in flight).
-    if (i >= 1 && i - 1 + stages < mine) {
-      ptx::bulk_wait_read<1>();
+    // Refill the stage of unit r = i-depth+1 once every lane's stores of unit
+    // r have read it; the store groups of the depth-1 later units stay in flight.
+    const int64_t r = i - depth + 1;
+    if (r >= 0 && r + stages < mine) {
+      wait_reads_at_most(depth - 1);
       __syncwarp();
-      if (lane == 0) issue_load(i - 1 + stages);
+      if (lane == 0) issue_load(r + stages);
     }
   }
   if (!ok) {
     if (lane == 0) {
       report(p.error_word, MOE_ETIMEDOUT);
       // Loads issued so far: the prologue's [0, prologue) and, from the
-      // refills of iterations 1..i-1, units up to i-2+stages.  Wait (bounded)
-      // for those not yet consumed before the CTA exits.
+      // refills of iterations up to i-1, units up to i-1-depth+1+stages.
+      // Wait (bounded) for those not yet consumed before the CTA exits.
       int64_t last = prologue - 1;
-      if (i >= 2 && i - 2 + stages > last) last = i - 2 + stages;
+      if (i - depth + stages > last) last = i - depth + stages;
       if (last > mine - 1) last = mine - 1;
       for (int64_t q = i; q <= last; ++q) wait_phase(&bars[q % stages], static_cast<uint32_t>((q / stages) & 1));
     }
@@ -190,6 +207,15 @@ __global__ void __launch_bounds__(256) dispatch_pack_vector(PackParams p) {
   }
 }
 
+// Store groups kept in flight before a stage is refilled: 1..min(8, stages-1)
+// (default 1: refill a stage as soon as its own stores have read it).
+int store_depth(int depth, int stages) {
+  if (depth < 1) depth = 1;
+  if (depth > 8) depth = 8;
+  if (depth > stages - 1) depth = stages - 1;
+  return depth < 1 ? 1 : depth;
+}
+
 }  // namespace
 
 size_t pack_bulk_smem_bytes(int stages, int piece_bytes) {
@@ -206,7 +232,7 @@ cudaError_t launch_dispatch_pack(const PackParams& p, const PackLaunch& l, cudaS
   }
   const int stages = l.stages < 2 ? 2 : (l.stages > kMaxStages ? kMaxStages : l.stages);
   return launch_kernel(dispatch_pack_bulk, dim3(l.grid), dim3(32), pack_bulk_smem_bytes(stages, p.piece_bytes),
-                       stream, l.pdl, p, stages, l.prefetch ? 1 : 0, l.hints);
+                       stream, l.pdl, p, stages, l.prefetch ? 1 : 0, l.hints, store_depth(l.depth, stages));
 }
 
 }  // namespace moe

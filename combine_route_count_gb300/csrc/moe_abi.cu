@@ -119,6 +119,7 @@ struct moe_ctx {
   int pack_ctas_per_sm;  // 0 = as many as fit
   int pack_prefetch;     // 1 = prefetch the CTA's later token rows into L2 before routing completes
   int cache_hints;       // MOE_OPT_CACHE_HINTS bit flags
+  int pack_depth;        // MOE_OPT_PACK_STORE_DEPTH (0 = default)
   int pdl;
   int route_variant;  // MOE_OPT_ROUTE_VARIANT
   int combine_variant;      // MOE_OPT_COMBINE_VARIANT
@@ -269,6 +270,10 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       if (value < 0 || value > 7) return MOE_EINVAL;
       ctx->cache_hints = static_cast<int>(value);
       return MOE_OK;
+    case MOE_OPT_PACK_STORE_DEPTH:
+      if (value < 0 || value > 8) return MOE_EINVAL;
+      ctx->pack_depth = static_cast<int>(value);
+      return MOE_OK;
     case MOE_OPT_COMBINE_VARIANT:
       if (value != moe::kCombineBulk && value != moe::kCombineVector) return MOE_EINVAL;
       ctx->combine_variant = static_cast<int>(value);
@@ -319,6 +324,9 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
     case MOE_OPT_CACHE_HINTS:
       *value = ctx->cache_hints;
       return MOE_OK;
+    case MOE_OPT_PACK_STORE_DEPTH:
+      *value = ctx->pack_depth;
+      return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       *value = ctx->route_variant != 0 ? ctx->route_variant : (ctx->cluster_ctas > 0 ? 3 : 2);
       return MOE_OK;
@@ -357,9 +365,10 @@ int pack_piece_bytes(const moe_ctx* c, int64_t row_bytes) {
 }
 
 int pack_grid(const moe_ctx* c, const moe::PackParams& p, int stages) {
+  const bool bulk = c->pack_variant == moe::kPackBulk;
   const int64_t units = static_cast<int64_t>(p.T) * p.pieces;
-  int per_sm = c->pack_ctas_per_sm > 0 ? c->pack_ctas_per_sm : (c->pack_variant == moe::kPackBulk ? 2 : 0);
-  if (c->pack_variant == moe::kPackBulk) {
+  int per_sm = c->pack_ctas_per_sm > 0 ? c->pack_ctas_per_sm : (bulk ? 2 : 0);
+  if (bulk) {
     const size_t smem = moe::pack_bulk_smem_bytes(stages, p.piece_bytes);
     // 228 KiB of shared memory per SM, 1 KiB of it reserved per resident CTA.
     const int fit = static_cast<int>((228 * 1024) / (smem + 1024));
@@ -369,7 +378,7 @@ int pack_grid(const moe_ctx* c, const moe::PackParams& p, int stages) {
     per_sm = 8;  // 8 x 256 threads
   }
   int64_t grid = static_cast<int64_t>(c->num_sms) * per_sm;
-  const int64_t useful = c->pack_variant == moe::kPackBulk ? units : (units + 7) / 8;
+  const int64_t useful = bulk ? units : (units + 7) / 8;
   if (grid > useful) grid = useful;
   if (grid < 1) grid = 1;
   return static_cast<int>(grid);
@@ -480,6 +489,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     pl.pdl = ctx->pdl != 0;
     pl.prefetch = ctx->pack_prefetch != 0;
     pl.hints = ctx->cache_hints;
+    pl.depth = ctx->pack_depth;
     if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
   }
   ctx->phase = kDispatched;

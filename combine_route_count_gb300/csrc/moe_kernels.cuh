@@ -95,6 +95,7 @@ struct PackLaunch {
   bool pdl;       // launch with programmatic stream serialization
   bool prefetch;  // bulk: prefetch the CTA's later rows into L2 in the prologue
   int hints;      // CacheHints
+  int depth;      // bulk: store groups in flight before a stage is refilled (0 = default 1)
 };
 size_t pack_bulk_smem_bytes(int stages, int piece_bytes);
 cudaError_t prepare_pack(int max_smem_bytes);  // one-time per-device attribute setup

@@ -155,6 +155,7 @@ MOE_API int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, cons
   pl.pdl = true;
   pl.prefetch = false;
   pl.hints = 0;
+  pl.depth = 0;
   if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
   return MOE_OK;
 }

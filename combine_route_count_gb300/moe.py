@@ -29,6 +29,7 @@ MOE_OPT_COMBINE_VARIANT, MOE_OPT_COMBINE_STAGES, MOE_OPT_COMBINE_PIECE_BYTES, MO
 COMBINE_BULK, COMBINE_VECTOR = 0, 1
 MOE_OPT_PACK_PREFETCH = 12
 MOE_OPT_CACHE_HINTS = 13
+MOE_OPT_PACK_STORE_DEPTH = 14
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.
@@ -272,7 +273,7 @@ class MoELayer:
                  "combine_variant": MOE_OPT_COMBINE_VARIANT, "combine_stages": MOE_OPT_COMBINE_STAGES,
                  "combine_piece_bytes": MOE_OPT_COMBINE_PIECE_BYTES,
                  "combine_ctas_per_sm": MOE_OPT_COMBINE_CTAS_PER_SM, "pack_prefetch": MOE_OPT_PACK_PREFETCH,
-                 "cache_hints": MOE_OPT_CACHE_HINTS}
+                 "cache_hints": MOE_OPT_CACHE_HINTS, "pack_store_depth": MOE_OPT_PACK_STORE_DEPTH}
         for k, v in options.items():
             moe_ctx_set_option(self.ctx, names[k], int(v))
 

@@ -199,6 +199,9 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               loads, 2 = pack stores, 4 = combine loads
  *                               (default 7: all streamed data) */
 #define MOE_OPT_CACHE_HINTS 13
+/*   MOE_OPT_PACK_STORE_DEPTH    bulk pack: store groups left in flight before a
+ *                               stage is refilled, 1..8 (0 = default, 1) */
+#define MOE_OPT_PACK_STORE_DEPTH 14
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
 /* ---- Dispatch without any device allocation ------------------------------

@@ -161,6 +161,8 @@ PACK_OPTIONS = [
     dict(cache_hints=0, pack_prefetch=0),
     dict(cache_hints=5, pack_prefetch=1, pack_stages=16, pack_ctas_per_sm=1),
     dict(pack_stages=14, pack_ctas_per_sm=2, combine_stages=5),
+    dict(pack_store_depth=1),
+    dict(pack_store_depth=5, pack_stages=6),
 ]
 
 
@@ -191,17 +193,18 @@ EDGE = [
 ]
 
 
-VARIANTS = [(0, 0), (1, 1), (2, 0)]  # (route_variant, combine_variant)
+VARIANTS = [(0, 0, 0), (1, 1, 1), (2, 0, 0)]  # (route_variant, combine_variant, pack_variant)
 
 
-@pytest.mark.parametrize("variants", VARIANTS, ids=["cluster-bulk", "single-vector", "split-bulk"])
+@pytest.mark.parametrize("variants", VARIANTS, ids=["cluster-bulk-bulk", "single-vector-vector", "split-bulk-bulk"])
 @pytest.mark.parametrize("shape", EDGE, ids=["x".join(map(str, s[:5])) for s in EDGE])
 def test_edge_shapes(moe, oracle_mod, shape, variants):
     T, H, K, E, N, router = shape
     w = gen.custom("edge", T=T, H=H, K=K, E=E, N=N, router=router, seed_index=11)
     li = gen.make_inputs(w)
     d, out_ref = oracle_of(oracle_mod, w, li)
-    res = run_gpu(moe, w, li, extra_rows=5, route_variant=variants[0], combine_variant=variants[1])
+    res = run_gpu(moe, w, li, extra_rows=5, route_variant=variants[0], combine_variant=variants[1],
+                  pack_variant=variants[2])
     assert_parity(res, d, out_ref, w, extra_rows=5)
 
 
@@ -231,7 +234,7 @@ def test_non_default_stream_and_reuse(moe, oracle_mod):
         assert_parity(res, d, out_ref, w)
 
 
-@pytest.mark.parametrize("variants", VARIANTS, ids=["cluster-bulk", "single-vector", "split-bulk"])
+@pytest.mark.parametrize("variants", VARIANTS, ids=["cluster-bulk-bulk", "single-vector-vector", "split-bulk-bulk"])
 @pytest.mark.parametrize("bad", ["out_of_range", "negative", "repeated"])
 def test_routing_errors_write_nothing(moe, bad, variants):
     w = gen.custom("bad", T=300, H=64, K=4, E=16, N=4, seed_index=3)
@@ -244,7 +247,7 @@ def test_routing_errors_write_nothing(moe, bad, variants):
     else:
         idx[299, 3] = idx[299, 1]
     li2 = gen.LayerInputs(w, li.x, idx, li.topk_w, li.y)
-    res = run_gpu(moe, w, li2, route_variant=variants[0], combine_variant=variants[1])
+    res = run_gpu(moe, w, li2, route_variant=variants[0], combine_variant=variants[1], pack_variant=variants[2])
     assert res["status"] == moe.MOE_EROUTE
     assert res["error_word"][0] == moe.MOE_EROUTE
     assert res["guards_ok"]
