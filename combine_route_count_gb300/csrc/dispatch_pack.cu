@@ -71,7 +71,7 @@ __device__ __forceinline__ void report(int32_t* error_word, int status) {
 }
 
 __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stages, int prefetch, int hints,
-                                                          int depth) {
+                                                          int depth, int prefetch_units) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* stage_buf = smem + kBarBytes;
@@ -112,13 +112,25 @@ __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stage
   const int64_t prologue = mine < stages ? mine : stages;
   if (lane == 0)
     for (int64_t i = 0; i < prologue; ++i) issue_load(i);
+  // At most prefetch_units units past the prologue (the soonest needed), so
+  // that the prefetched rows fit in L2 next to the write stream.
+  const int64_t pf_end =
+      !prefetch ? prologue : (prefetch_units < 0 || prologue + prefetch_units > mine ? mine : prologue + prefetch_units);
   if (prefetch) {
     // The later rows of this CTA go to L2 now, while routing still runs.
-    for (int64_t i = prologue + lane; i < mine; i += 32) {
+    // prefetch == 2 marks them evict-last so that the write stream of this
+    // kernel does not push them out before they are loaded; each piece is
+    // handed back to normal priority as soon as it has been loaded.
+    const uint64_t keep = prefetch == 2 ? ptx::policy_evict_last() : 0;
+    for (int64_t i = prologue + lane; i < pf_end; i += 32) {
       const int64_t u = first + i * step;
       const int64_t t = u / p.pieces;
       const int j = static_cast<int>(u - t * p.pieces);
-      ptx::bulk_prefetch_l2(p.x + t * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes, piece_bytes(j));
+      const uint8_t* src = p.x + t * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes;
+      if (prefetch == 2)
+        ptx::bulk_prefetch_l2_hint(src, piece_bytes(j), keep);
+      else
+        ptx::bulk_prefetch_l2(src, piece_bytes(j));
     }
   }
 
@@ -138,6 +150,13 @@ __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stage
     if (!__all_sync(0xffffffffu, arrived)) {
       ok = false;
       break;
+    }
+    if (prefetch == 2 && i >= prologue && i < pf_end) {
+      // This piece was prefetched evict-last; it is in shared memory now, so
+      // hand its L2 lines back to normal priority.
+      const uint8_t* src = p.x + t * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes;
+      const uint32_t lines = (piece_bytes(j) + 127) / 128;
+      for (uint32_t q = lane; q < lines; q += 32) ptx::l2_priority_normal(src + static_cast<size_t>(q) * 128);
     }
     if (row >= 0) {
       uint8_t* dst = p.expert_x + static_cast<int64_t>(row) * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes;
@@ -232,7 +251,7 @@ cudaError_t launch_dispatch_pack(const PackParams& p, const PackLaunch& l, cudaS
   }
   const int stages = l.stages < 2 ? 2 : (l.stages > kMaxStages ? kMaxStages : l.stages);
   return launch_kernel(dispatch_pack_bulk, dim3(l.grid), dim3(32), pack_bulk_smem_bytes(stages, p.piece_bytes),
-                       stream, l.pdl, p, stages, l.prefetch ? 1 : 0, l.hints, store_depth(l.depth, stages));
+                       stream, l.pdl, p, stages, l.prefetch, l.hints, store_depth(l.depth, stages), l.prefetch_units);
 }
 
 }  // namespace moe

@@ -100,6 +100,7 @@ struct moe_ctx {
   int device;
   int num_sms;
   int max_smem_optin;
+  int l2_bytes;
   int phase;
   const void* expert_y;
   int64_t expert_y_rows;
@@ -175,6 +176,8 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ECUDA;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ECUDA;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return MOE_ECUDA;
+  int l2 = 0;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return MOE_ECUDA;
   if (moe::route_count_smem_bytes(cfg->num_experts) > static_cast<size_t>(optin)) return MOE_EINVAL;
   if (moe::route_local_smem_bytes(cfg->num_experts) > static_cast<size_t>(optin)) return MOE_EINVAL;
   if (moe::prepare_pack(optin) != cudaSuccess) return MOE_ECUDA;
@@ -188,6 +191,7 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->device = dev;
   c->num_sms = sms;
   c->max_smem_optin = optin;
+  c->l2_bytes = l2;
   c->phase = kIdle;
   c->error_word = reinterpret_cast<int32_t*>(c->ws + l.error_word);
   c->expert_counts = reinterpret_cast<int32_t*>(c->ws + l.expert_counts);
@@ -200,7 +204,7 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->block_err = reinterpret_cast<int32_t*>(c->ws + l.block_err);
   c->pack_variant = moe::kPackBulk;
   c->pack_stages = 0;  // automatic: about 100 KiB of stages per CTA
-  c->pack_prefetch = 1;
+  c->pack_prefetch = 2;
   c->cache_hints = moe::kHintPackLoads | moe::kHintPackStores | moe::kHintCombineLoads;
   c->pack_piece_bytes = 0;
   c->pack_ctas_per_sm = 0;
@@ -263,7 +267,7 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       ctx->pdl = static_cast<int>(value);
       return MOE_OK;
     case MOE_OPT_PACK_PREFETCH:
-      if (value != 0 && value != 1) return MOE_EINVAL;
+      if (value < 0 || value > 2) return MOE_EINVAL;
       ctx->pack_prefetch = static_cast<int>(value);
       return MOE_OK;
     case MOE_OPT_CACHE_HINTS:
@@ -399,7 +403,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  moe::RouteCountParams rp;
+  moe::RouteCountParams rp = {};
   rp.topk_idx = topk_idx;
   rp.T = c.num_tokens;
   rp.K = c.top_k;
@@ -419,7 +423,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
   if (ctx->route_variant == 1) {
     if (moe::launch_route_count(rp, vec, s) != cudaSuccess) return MOE_ECUDA;
   } else if (use_cluster) {
-    moe::RouteClusterParams cp;
+    moe::RouteClusterParams cp = {};
     cp.topk_idx = topk_idx;
     cp.T = c.num_tokens;
     cp.K = c.top_k;
@@ -438,7 +442,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     cp.error_word = ctx->error_word;
     if (moe::launch_route_cluster(cp, vec, ctx->cluster_ctas, s) != cudaSuccess) return MOE_ECUDA;
   } else {
-    moe::RouteSplitParams sp;
+    moe::RouteSplitParams sp = {};
     sp.topk_idx = topk_idx;
     sp.T = c.num_tokens;
     sp.K = c.top_k;
@@ -458,7 +462,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
   }
 
   if (c.num_tokens > 0) {
-    moe::PackParams pp;
+    moe::PackParams pp = {};
     pp.x = static_cast<const uint8_t*>(x);
     pp.expert_x = static_cast<uint8_t*>(expert_x);
     pp.slot_row = ctx->slot_row;
@@ -468,7 +472,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     pp.row_bytes = static_cast<int64_t>(c.hidden) * 2;
     pp.piece_bytes = pack_piece_bytes(ctx, pp.row_bytes);
     pp.pieces = static_cast<int32_t>((pp.row_bytes + pp.piece_bytes - 1) / pp.piece_bytes);
-    moe::PackLaunch pl;
+    moe::PackLaunch pl = {};
     pl.variant = ctx->pack_variant;
     pl.stages = ctx->pack_stages;
     if (pl.stages <= 0) {
@@ -486,8 +490,26 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
         return MOE_EINVAL;
     }
     pl.grid = pack_grid(ctx, pp, pl.stages);
+    pl.prefetch = ctx->pack_prefetch;
+    pl.prefetch_units = -1;
+    if (pl.prefetch == 2) {
+      // Evict-last prefetch when every row a CTA still needs after its
+      // prologue fits, across the grid, in a third of L2.  (Measured on
+      // GB300: it pays at DeepSeek size even beyond the device's persisting
+      // L2 carve-out, so that carve-out does not bound it.)
+      const int64_t budget = static_cast<int64_t>(ctx->l2_bytes) / 3;
+      const int64_t units = static_cast<int64_t>(pp.T) * pp.pieces;
+      const int64_t per_cta = (units + pl.grid - 1) / pl.grid - pl.stages;  // units past the prologue
+      const int64_t fit = budget > 0 ? budget / (static_cast<int64_t>(pl.grid) * pp.piece_bytes) : 0;
+      if (per_cta > 0 && fit >= per_cta) {
+        pl.prefetch_units = static_cast<int>(per_cta);
+      } else {
+        // The token rows do not fit: marking part of them evict-last was
+        // measured slower (Kimi-sized layers) than prefetching all normally.
+        pl.prefetch = 1;
+      }
+    }
     pl.pdl = ctx->pdl != 0;
-    pl.prefetch = ctx->pack_prefetch != 0;
     pl.hints = ctx->cache_hints;
     pl.depth = ctx->pack_depth;
     if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
@@ -534,7 +556,7 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
   const moe_config& c = ctx->cfg;
   if (c.num_tokens > 0) {
     if (!topk_w || !out || !aligned(topk_w, 4) || !aligned(out, 16)) return MOE_EINVAL;
-    moe::CombineParams cp;
+    moe::CombineParams cp = {};
     cp.y = static_cast<const uint8_t*>(ctx->expert_y);
     cp.w = topk_w;
     cp.slot_row = ctx->slot_row;
@@ -543,7 +565,7 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
     cp.K = c.top_k;
     cp.H = c.hidden;
     cp.error_word = ctx->error_word;
-    moe::CombineLaunch cl;
+    moe::CombineLaunch cl = {};
     cl.pdl = ctx->pdl != 0;
     cl.variant = ctx->combine_variant;
     cl.grid = 0;

@@ -93,9 +93,10 @@ struct PackLaunch {
   int grid;       // CTAs
   int stages;     // bulk: shared-memory stages per CTA (2..8)
   bool pdl;       // launch with programmatic stream serialization
-  bool prefetch;  // bulk: prefetch the CTA's later rows into L2 in the prologue
+  int prefetch;   // bulk: 0 = off, 1 = prefetch the CTA's later rows into L2 in the prologue, 2 = same, evict-last
   int hints;      // CacheHints
   int depth;      // bulk: store groups in flight before a stage is refilled (0 = default 1)
+  int prefetch_units;  // bulk: units past the prologue each CTA prefetches (-1 = all)
 };
 size_t pack_bulk_smem_bytes(int stages, int piece_bytes);
 cudaError_t prepare_pack(int max_smem_bytes);  // one-time per-device attribute setup

@@ -107,7 +107,7 @@ MOE_API int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, cons
   int32_t* rank_offsets = src_offsets + kMaxExpertRanks;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  moe::RouteCountParams rp;
+  moe::RouteCountParams rp = {};
   rp.topk_idx = topk_idx;
   rp.T = cfg->num_tokens;
   rp.K = cfg->top_k;
@@ -126,7 +126,7 @@ MOE_API int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, cons
   if (moe::launch_route_count(rp, vec, s) != cudaSuccess) return MOE_ECUDA;
   if (cfg->num_tokens == 0) return MOE_OK;
 
-  moe::PackParams pp;
+  moe::PackParams pp = {};
   pp.x = static_cast<const uint8_t*>(x);
   pp.expert_x = static_cast<uint8_t*>(expert_x);
   pp.slot_row = slot_row;
@@ -139,7 +139,7 @@ MOE_API int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, cons
   const int64_t npieces = (pp.row_bytes + 16384 - 1) / 16384;
   pp.piece_bytes = static_cast<int32_t>((pp.row_bytes / 16 + npieces - 1) / npieces * 16);
   pp.pieces = static_cast<int32_t>((pp.row_bytes + pp.piece_bytes - 1) / pp.piece_bytes);
-  moe::PackLaunch pl;
+  moe::PackLaunch pl = {};
   pl.variant = moe::kPackBulk;
   pl.stages = 4;
   while (pl.stages > 2 && moe::pack_bulk_smem_bytes(pl.stages, pp.piece_bytes) > static_cast<size_t>(ds.max_smem_optin))
@@ -153,7 +153,8 @@ MOE_API int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, cons
   if (grid > units) grid = units;
   pl.grid = static_cast<int>(grid);
   pl.pdl = true;
-  pl.prefetch = false;
+  pl.prefetch = 0;
+  pl.prefetch_units = 0;
   pl.hints = 0;
   pl.depth = 0;
   if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;

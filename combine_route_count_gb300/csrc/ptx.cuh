@@ -96,6 +96,14 @@ __device__ __forceinline__ void bulk_s2g_hint(void* gmem_dst, const void* smem_s
 __device__ __forceinline__ void bulk_prefetch_l2(const void* gmem_src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem_src), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void bulk_prefetch_l2_hint(const void* gmem_src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(gmem_src), "r"(bytes), "l"(pol)
+               : "memory");
+}
+// Resets the L2 eviction priority of the 128-byte line at `gmem` to normal.
+__device__ __forceinline__ void l2_priority_normal(const void* gmem) {
+  asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(gmem) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's committed groups still read shared memory.
 template <int N>

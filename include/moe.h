@@ -192,8 +192,12 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
 #define MOE_OPT_COMBINE_STAGES 9
 #define MOE_OPT_COMBINE_PIECE_BYTES 10
 #define MOE_OPT_COMBINE_CTAS_PER_SM 11
-/*   MOE_OPT_PACK_PREFETCH       bulk pack: 1 = prefetch each CTA's later token
- *                               rows into L2 while routing runs (default), 0 = off */
+/*   MOE_OPT_PACK_PREFETCH       bulk pack: while routing runs, each CTA
+ *                               prefetches its later token rows into L2:
+ *                               2 = with an evict-last policy when all of them
+ *                               fit in a third of L2, else as 1 (default); each
+ *                               row goes back to normal priority once loaded;
+ *                               1 = all of them with normal priority; 0 = off */
 #define MOE_OPT_PACK_PREFETCH 12
 /*   MOE_OPT_CACHE_HINTS         bit flags, L2 evict-first policy on: 1 = pack
  *                               loads, 2 = pack stores, 4 = combine loads
