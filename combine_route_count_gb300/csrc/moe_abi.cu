@@ -210,7 +210,7 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->pack_ctas_per_sm = 0;
   c->pdl = 1;
   c->route_variant = 0;
-  c->combine_variant = moe::kCombineBulk;
+  c->combine_variant = -1;  // automatic
   // Largest cluster of route_cluster CTAs this device can schedule for this
   // configuration (16, else 8, 4, 2, 1), or none.
   for (int maxc = moe::kMaxClusterCtas; maxc >= 1; maxc /= 2) {
@@ -242,6 +242,20 @@ MOE_API int moe_ctx_destroy(moe_ctx* ctx) {
   delete ctx;
   return MOE_OK;
 }
+
+namespace {
+
+// Automatic choices, from steady-state sweeps on GB300: with K >= 4 the TMA
+// gather combine and 2 pack CTAs per SM are fastest (DeepSeek, Kimi, worst
+// case); with K <= 2 each unit carries too little work for the bulk combine's
+// per-CTA pipeline and 3 pack CTAs per SM issue faster (Mixtral).
+int combine_variant_of(const moe_ctx* c) {
+  if (c->combine_variant >= 0) return c->combine_variant;
+  return c->cfg.top_k >= 4 ? moe::kCombineBulk : moe::kCombineVector;
+}
+int pack_ctas_auto(const moe_ctx* c) { return c->cfg.top_k >= 4 ? 2 : 3; }
+
+}  // namespace
 
 MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
   if (!ctx) return MOE_EINVAL;
@@ -279,7 +293,7 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       ctx->pack_depth = static_cast<int>(value);
       return MOE_OK;
     case MOE_OPT_COMBINE_VARIANT:
-      if (value != moe::kCombineBulk && value != moe::kCombineVector) return MOE_EINVAL;
+      if (value != -1 && value != moe::kCombineBulk && value != moe::kCombineVector) return MOE_EINVAL;
       ctx->combine_variant = static_cast<int>(value);
       return MOE_OK;
     case MOE_OPT_COMBINE_STAGES:
@@ -338,7 +352,7 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
       *value = ctx->cluster_ctas;
       return MOE_OK;
     case MOE_OPT_COMBINE_VARIANT:
-      *value = ctx->combine_variant;
+      *value = combine_variant_of(ctx);
       return MOE_OK;
     case MOE_OPT_COMBINE_STAGES:
       *value = ctx->combine_stages;
@@ -371,7 +385,7 @@ int pack_piece_bytes(const moe_ctx* c, int64_t row_bytes) {
 int pack_grid(const moe_ctx* c, const moe::PackParams& p, int stages) {
   const bool bulk = c->pack_variant == moe::kPackBulk;
   const int64_t units = static_cast<int64_t>(p.T) * p.pieces;
-  int per_sm = c->pack_ctas_per_sm > 0 ? c->pack_ctas_per_sm : (bulk ? 2 : 0);
+  int per_sm = c->pack_ctas_per_sm > 0 ? c->pack_ctas_per_sm : (bulk ? pack_ctas_auto(c) : 0);
   if (bulk) {
     const size_t smem = moe::pack_bulk_smem_bytes(stages, p.piece_bytes);
     // 228 KiB of shared memory per SM, 1 KiB of it reserved per resident CTA.
@@ -477,7 +491,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     pl.stages = ctx->pack_stages;
     if (pl.stages <= 0) {
       // About 100 KiB of stages per CTA (two CTAs per SM), 2..16 stages.
-      pl.stages = static_cast<int>((100 * 1024) / pp.piece_bytes);
+      pl.stages = static_cast<int>((200 * 1024) / pack_ctas_auto(ctx) / pp.piece_bytes);
       if (pl.stages > 16) pl.stages = 16;
       if (pl.stages < 2) pl.stages = 2;
     }
@@ -567,7 +581,7 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
     cp.error_word = ctx->error_word;
     moe::CombineLaunch cl = {};
     cl.pdl = ctx->pdl != 0;
-    cl.variant = ctx->combine_variant;
+    cl.variant = combine_variant_of(ctx);
     cl.grid = 0;
     if (cl.variant == moe::kCombineBulk) {
       cl.shape = moe::combine_bulk_shape(c.hidden, c.top_k, ctx->combine_stages, ctx->combine_piece_bytes,

@@ -155,11 +155,12 @@ int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void* stream)
  *   MOE_OPT_PACK_VARIANT      0 = bulk copies through shared memory (TMA
  *                             engine, default), 1 = 16-byte vector loads/stores
  *   MOE_OPT_PACK_STAGES       shared-memory stages per bulk CTA, 2..16, 0 =
- *                             automatic (about 100 KiB of stages, default)
+ *                             automatic (about 200 KiB of stages per SM, default)
  *   MOE_OPT_PACK_PIECE_BYTES  bytes of a row moved per work unit, a multiple of
  *                             16, 0 = automatic (whole row up to 8 KiB, else
  *                             equal pieces of at most 8 KiB)
- *   MOE_OPT_PACK_CTAS_PER_SM  0 = automatic (2 for the bulk variant), else 1..32
+ *   MOE_OPT_PACK_CTAS_PER_SM  0 = automatic (bulk variant: 2 for K >= 4, else 3),
+ *                             else 1..32
  *   MOE_OPT_PDL               1 = launch pack/combine with programmatic
  *                             dependent launch (default), 0 = plain launches
  *   MOE_OPT_ROUTE_VARIANT     routing kernels: 0 = automatic (route_cluster
@@ -183,8 +184,9 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
 #define MOE_OPT_ROUTE_CLUSTER_CTAS 7
 /*   MOE_OPT_COMBINE_VARIANT     0 = a producer warp gathers the K expert-row
  *                               pieces with bulk copies into shared-memory
- *                               stages, consumer warps reduce (default);
- *                               1 = one thread per 16-byte chunk, direct loads
+ *                               stages, consumer warps reduce; 1 = one thread
+ *                               per 16-byte chunk, direct loads; -1 = automatic
+ *                               (default: 0 for K >= 4, else 1)
  *   MOE_OPT_COMBINE_STAGES      bulk: stages per CTA, 2..8, 0 = automatic
  *   MOE_OPT_COMBINE_PIECE_BYTES bulk: bytes of a row per unit, 0 = automatic
  *   MOE_OPT_COMBINE_CTAS_PER_SM bulk: 0 = as many as fit, else 1..32 */
