@@ -64,6 +64,12 @@ def _load() -> ctypes.CDLL:
         lib.oracle_double_to_bf16.restype = ctypes.c_uint16
         lib.oracle_fmaf.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float]
         lib.oracle_fmaf.restype = ctypes.c_float
+        lib.oracle_quantize_fp8.argtypes = [i32, i32, p, p, p]
+        lib.oracle_quantize_fp8.restype = ctypes.c_int
+        lib.oracle_float_to_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = ctypes.c_double
         _lib = lib
     return _lib
 
@@ -160,3 +166,38 @@ def double_to_bf16(v: float) -> int:
 
 def fmaf(a: float, b: float, c: float) -> float:
     return float(_load().oracle_fmaf(a, b, c))
+
+
+FP8_BLOCK = 128
+
+
+def quantize_fp8(x: np.ndarray):
+    """Block-scaled fp8 (E4M3) payload of bf16 rows: (q uint8 [T, H],
+    scales float32 [T, H/128]); see ``oracle_quantize_fp8``."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T, H = x.shape
+    q = np.zeros((T, H), dtype=np.uint8)
+    sc = np.zeros((T, H // FP8_BLOCK), dtype=np.float32)
+    rc = lib.oracle_quantize_fp8(T, H, _ptr(x), _ptr(q), _ptr(sc))
+    if rc != OK:
+        raise OracleError(rc, "oracle_quantize_fp8")
+    return q, sc
+
+
+def dispatch_fp8(x: np.ndarray, topk_idx: np.ndarray, E: int, N: int):
+    """fp8 dispatch: the placement of ``dispatch`` applied to the quantised
+    rows.  Returns (Dispatch, expert_xq uint8 [T*K, H], expert_scales
+    float32 [T*K, H/128])."""
+    d = dispatch(x, topk_idx, E, N)
+    q, sc = quantize_fp8(x)
+    src = d.row_src // max(topk_idx.shape[1], 1)
+    return d, q[src], sc[src]
+
+
+def float_to_e4m3(f: float) -> int:
+    return int(_load().oracle_float_to_e4m3(f))
+
+
+def e4m3_to_double(b: int) -> float:
+    return float(_load().oracle_e4m3_to_double(b))

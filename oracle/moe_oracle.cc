@@ -40,6 +40,13 @@
 //    not renormalised by the sum of weights.
 //  * A second combine evaluates the same sum in double precision and rounds it
 //    once to bf16: the plain mathematical definition, for error bounds.
+//  * fp8 dispatch payload ("Efficient and portable mixture-of-experts
+//    communication", Dispatch: tokens travel with block scaling factors;
+//    "Enabling trillion-parameter models on AWS EFA", evaluation: block-scale
+//    fp8 dispatch, bf16 combine).  The pages give neither the block nor the
+//    scale rule; read as blocks of 128 consecutive elements of a row, E4M3,
+//    scale = amax/448 so the largest element maps to the largest finite code,
+//    q = round-to-nearest-even(x / scale), saturating.
 //
 // All bf16 values are raw 16-bit patterns.
 
@@ -98,6 +105,45 @@ uint16_t double_to_bf16_rne(double v) {
   std::memcpy(&u, &f, sizeof u);
   return static_cast<uint16_t>(u >> 16);
 }
+
+// fp8 E4M3 ("FN" variant: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+// bits, no infinities, S.1111.111 is NaN, largest finite 448).  Round to
+// nearest, ties to even, saturating to +-448 (finite inputs only).
+uint8_t float_to_e4m3_rne_sat(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  const uint8_t sign = static_cast<uint8_t>((u >> 24) & 0x80u);
+  if ((u & 0x7f800000u) == 0x7f800000u) return static_cast<uint8_t>(sign | 0x7f);  // NaN/Inf: NaN
+  const double a = std::fabs(static_cast<double>(f));
+  if (a >= 448.0) return static_cast<uint8_t>(sign | 0x7e);
+  if (a < std::ldexp(1.0, -6)) {
+    // Subnormal range: multiples of 2^-9 (a code of 8 is the smallest normal).
+    const double m = std::nearbyint(a * 512.0);  // exact scaling; ties to even
+    return static_cast<uint8_t>(sign | static_cast<uint8_t>(m));  // m <= 8: 0b0000.mmm or 0b0001.000
+  }
+  int e;
+  std::frexp(a, &e);  // a = f * 2^e, f in [0.5, 1): unbiased exponent e-1
+  int ex = e - 1;
+  double m = std::nearbyint(std::ldexp(a, 3 - ex));  // in [8, 16]
+  if (m >= 16.0) {
+    m = 8.0;
+    ++ex;
+  }
+  if (ex > 8) return static_cast<uint8_t>(sign | 0x7e);
+  const uint8_t code = static_cast<uint8_t>(((ex + 7) << 3) | (static_cast<int>(m) - 8));
+  return static_cast<uint8_t>(sign | (code > 0x7e ? 0x7e : code));
+}
+
+double e4m3_to_double(uint8_t b) {
+  const int sign = (b & 0x80) ? -1 : 1;
+  const int ex = (b >> 3) & 0xf, man = b & 0x7;
+  if (ex == 0xf && man == 0x7) return std::nan("");
+  if (ex == 0) return sign * std::ldexp(static_cast<double>(man), -9);
+  return sign * std::ldexp(static_cast<double>(8 + man), ex - 10);
+}
+
+constexpr int kFp8Block = 128;  // elements per scaling block
+constexpr float kE4m3Max = 448.0f;
 
 int check_sizes(int32_t T, int32_t H, int32_t K, int32_t E, int32_t N) {
   if (T < 0 || H < 1 || K < 1 || E < 1 || N < 1) return ORACLE_EINVAL;
@@ -265,9 +311,35 @@ int oracle_combine_f64(int32_t T, int32_t H, int32_t K, const uint16_t* y, int64
   return ORACLE_OK;
 }
 
+// Block-scaled fp8 quantisation of token rows (the dispatch payload with
+// "block scaling factors"): for each row and each block of 128 consecutive
+// elements, scale = amax / 448 (1 for an all-zero block), computed in float32,
+// and q = e4m3_rne_sat(x / scale) with a float32 division.
+//   x       bf16 [T, H], H % 128 == 0
+//   q       e4m3 [T, H]
+//   scales  float32 [T, H/128]
+int oracle_quantize_fp8(int32_t T, int32_t H, const uint16_t* x, uint8_t* q, float* scales) {
+  if (T < 0 || H < kFp8Block || H % kFp8Block != 0) return ORACLE_EINVAL;
+  const int32_t nb = H / kFp8Block;
+  for (int64_t t = 0; t < T; ++t) {
+    for (int32_t b = 0; b < nb; ++b) {
+      const uint16_t* blk = x + t * H + static_cast<int64_t>(b) * kFp8Block;
+      float amax = 0.0f;
+      for (int i = 0; i < kFp8Block; ++i) amax = std::max(amax, std::fabs(bf16_to_float(blk[i])));
+      const float scale = amax > 0.0f ? amax / kE4m3Max : 1.0f;
+      scales[t * nb + b] = scale;
+      for (int i = 0; i < kFp8Block; ++i)
+        q[t * H + static_cast<int64_t>(b) * kFp8Block + i] = float_to_e4m3_rne_sat(bf16_to_float(blk[i]) / scale);
+    }
+  }
+  return ORACLE_OK;
+}
+
 // Element-wise helpers exposed for the pins.
 uint16_t oracle_float_to_bf16(float f) { return float_to_bf16_rne(f); }
 uint16_t oracle_double_to_bf16(double v) { return double_to_bf16_rne(v); }
 float oracle_fmaf(float a, float b, float c) { return std::fmaf(a, b, c); }
+uint8_t oracle_float_to_e4m3(float f) { return float_to_e4m3_rne_sat(f); }
+double oracle_e4m3_to_double(uint8_t b) { return e4m3_to_double(b); }
 
 }  // extern "C"
