@@ -41,19 +41,23 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--buffer-sets", type=int, default=2)
+    ap.add_argument("--payload", choices=["bf16", "fp8"], default="bf16",
+                    help="dispatch payload: bf16 rows, or block-scaled fp8 rows (moe_dispatch_send_fp8)")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step per buffer set in a CUDA graph and replay it")
     return ap.parse_args()
 
 
-def algorithmic_bytes(w):
+def algorithmic_bytes(w, payload="bf16"):
     """Bytes a layer must move at minimum (see the design notes):
-    dispatch reads x and writes T*K rows; combine reads T*K rows and writes T
-    rows; plus the routing metadata."""
+    dispatch reads x and writes T*K rows (bf16, or E4M3 bytes plus one float32
+    scale per 128 elements); combine reads T*K bf16 rows and writes T rows;
+    plus the routing metadata."""
     T, H, K, E, N = w.T, w.H, w.K, w.E, w.N
     row = H * 2
     pairs = T * K
-    dispatch = T * row + pairs * row
+    out_row = row if payload == "bf16" else H + (H // 128) * 4
+    dispatch = T * row + pairs * out_row
     dispatch_meta = 2 * pairs * 4 + 2 * pairs * 4 + pairs * 4 + (3 * E + E * N + N + 2) * 4
     combine = pairs * row + T * row
     combine_meta = pairs * 4 + pairs * 4
@@ -238,14 +242,23 @@ def run_gpu(args):
         y0 = torch.from_numpy(li.y.view(np.int16)).to(dev)
         for _ in range(args.buffer_sets):
             sets.append(dict(x=x0.clone(), idx=idx0.clone(), w=w0.clone(), y=y0.clone(),
-                             expert_x=torch.empty((rows, H), dtype=torch.int16, device=dev),
+                             expert_x=torch.empty((rows, H), dtype=torch.int16, device=dev)
+                             if args.payload == "bf16" else torch.empty((rows, H), dtype=torch.uint8, device=dev),
+                             expert_scales=None if args.payload == "bf16"
+                             else torch.empty((rows, H // 128), dtype=torch.float32, device=dev),
                              out=torch.empty((T, H), dtype=torch.int16, device=dev)))
         del x0, idx0, w0, y0
     torch.cuda.synchronize(dev)
     layer = moe.MoELayer(T, H, K, E, N, device=dev)
 
+    def dispatch(s):
+        if args.payload == "bf16":
+            layer.dispatch_send(s["x"], s["idx"], s["expert_x"], stream)
+        else:
+            layer.dispatch_send_fp8(s["x"], s["idx"], s["expert_x"], s["expert_scales"], stream)
+
     def step(s):
-        layer.dispatch_send(s["x"], s["idx"], s["expert_x"], stream)
+        dispatch(s)
         layer.dispatch_recv(stream)
         layer.combine_send(s["y"], stream)
         layer.combine_recv(s["w"], s["out"], stream)
@@ -317,7 +330,7 @@ def run_gpu(args):
     for i in range(n_attr):
         s = sets[i % len(sets)]
         ev[i][0].record(stream)
-        layer.dispatch_send(s["x"], s["idx"], s["expert_x"], stream)
+        dispatch(s)
         ev[i][1].record(stream)
         layer.dispatch_recv(stream)
         layer.combine_send(s["y"], stream)
@@ -328,7 +341,7 @@ def run_gpu(args):
     disp_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n_attr)]
     comb_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n_attr)]
 
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w, args.payload)
     peak, peak_kind = measured_peaks()
     disp_us = statistics.mean(disp_ms) * 1e3
     comb_us = statistics.mean(comb_ms) * 1e3
@@ -351,7 +364,7 @@ def run_gpu(args):
                 "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"}
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.payload == "bf16":
         e2e = run_e2e(args, w, li, layer, stream, dev)
 
     cpu = None
@@ -362,12 +375,14 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": round(us_layer, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if args.payload == "bf16" else "fp8-e4m3 dispatch / bf16 combine", "data": "synthetic",
             "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": f"inputs > L2: {ab['total'] / 1e6:.0f} MB moved per layer, "
                              f"{args.buffer_sets} rotating buffer sets",
                        "launch": "CUDA graph replay" if args.graph else "direct C-ABI calls",
+                       "payload": args.payload,
                        "pack": f"bulk (TMA), {layer.get_option(moe.MOE_OPT_PACK_STAGES) or 'auto'} stages, "
                                f"prefetch={layer.get_option(moe.MOE_OPT_PACK_PREFETCH)}, "
                                f"hints={layer.get_option(moe.MOE_OPT_CACHE_HINTS)}, PDL",

@@ -404,19 +404,12 @@ int pack_grid(const moe_ctx* c, const moe::PackParams& p, int stages) {
 
 }  // namespace
 
-MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_x,
-                              int64_t expert_x_rows, void* stream) {
-  if (!ctx) return MOE_EINVAL;
-  if (ctx->phase != kIdle) return MOE_ESTATE;
-  const moe_config& c = ctx->cfg;
-  const int64_t pairs = static_cast<int64_t>(c.num_tokens) * c.top_k;
-  if (expert_x_rows < pairs) return MOE_EINVAL;
-  if (c.num_tokens > 0) {
-    if (!x || !topk_idx || !expert_x) return MOE_EINVAL;
-    if (!aligned(x, 16) || !aligned(expert_x, 16) || !aligned(topk_idx, 4)) return MOE_EINVAL;
-  }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+namespace {
 
+// Enqueues the routing kernels of the context's variant (counts, offsets,
+// slot_row, row_src, error word).  MOE_OK or MOE_ECUDA.
+int enqueue_routing(moe_ctx* ctx, const int32_t* topk_idx, cudaStream_t s) {
+  const moe_config& c = ctx->cfg;
   moe::RouteCountParams rp = {};
   rp.topk_idx = topk_idx;
   rp.T = c.num_tokens;
@@ -474,6 +467,25 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     sp.block_err = ctx->block_err;
     if (moe::launch_route_split(sp, vec, s) != cudaSuccess) return MOE_ECUDA;
   }
+  return MOE_OK;
+}
+
+}  // namespace
+
+MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_x,
+                              int64_t expert_x_rows, void* stream) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->phase != kIdle) return MOE_ESTATE;
+  const moe_config& c = ctx->cfg;
+  const int64_t pairs = static_cast<int64_t>(c.num_tokens) * c.top_k;
+  if (expert_x_rows < pairs) return MOE_EINVAL;
+  if (c.num_tokens > 0) {
+    if (!x || !topk_idx || !expert_x) return MOE_EINVAL;
+    if (!aligned(x, 16) || !aligned(expert_x, 16) || !aligned(topk_idx, 4)) return MOE_EINVAL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rrc = enqueue_routing(ctx, topk_idx, s);
+  if (rrc != MOE_OK) return rrc;
 
   if (c.num_tokens > 0) {
     moe::PackParams pp = {};
@@ -527,6 +539,56 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     pl.hints = ctx->cache_hints;
     pl.depth = ctx->pack_depth;
     if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
+  }
+  ctx->phase = kDispatched;
+  return MOE_OK;
+}
+
+MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_xq,
+                                  float* expert_scales, int64_t expert_rows, void* stream) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->phase != kIdle) return MOE_ESTATE;
+  const moe_config& c = ctx->cfg;
+  const int64_t pairs = static_cast<int64_t>(c.num_tokens) * c.top_k;
+  if (c.hidden % MOE_FP8_BLOCK != 0 || expert_rows < pairs) return MOE_EINVAL;
+  // Two stages of one bf16 row must fit in shared memory.
+  if (moe::pack_fp8_smem_bytes(2, c.hidden) > static_cast<size_t>(ctx->max_smem_optin)) return MOE_EINVAL;
+  if (c.num_tokens > 0) {
+    if (!x || !topk_idx || !expert_xq || !expert_scales) return MOE_EINVAL;
+    if (!aligned(x, 16) || !aligned(expert_xq, 16) || !aligned(expert_scales, 4) || !aligned(topk_idx, 4))
+      return MOE_EINVAL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rrc = enqueue_routing(ctx, topk_idx, s);
+  if (rrc != MOE_OK) return rrc;
+  if (c.num_tokens > 0) {
+    moe::PackFp8Params fp = {};
+    fp.x = static_cast<const uint8_t*>(x);
+    fp.expert_xq = static_cast<uint8_t*>(expert_xq);
+    fp.expert_scales = expert_scales;
+    fp.slot_row = ctx->slot_row;
+    fp.error_word = ctx->error_word;
+    fp.T = c.num_tokens;
+    fp.K = c.top_k;
+    fp.H = c.hidden;
+    // MOE_OPT_PACK_STAGES / _CTAS_PER_SM apply here too; automatic: about
+    // 72 KiB of row stages per CTA, three CTAs (12 consumer warps) per SM.
+    int stages = ctx->pack_stages > 0 ? ctx->pack_stages
+                                      : static_cast<int>((72 * 1024) / (static_cast<int64_t>(c.hidden) * 2));
+    const int maxst = moe::pack_fp8_max_stages();
+    if (stages > maxst) stages = maxst;
+    if (stages < 2) stages = 2;
+    while (stages > 2 && moe::pack_fp8_smem_bytes(stages, c.hidden) > static_cast<size_t>(ctx->max_smem_optin))
+      --stages;
+    const size_t smem = moe::pack_fp8_smem_bytes(stages, c.hidden);
+    int per_sm = static_cast<int>((228 * 1024) / (smem + 1024));
+    const int want = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : 3;
+    if (per_sm > want) per_sm = want;
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = static_cast<int64_t>(ctx->num_sms) * per_sm;
+    if (grid > c.num_tokens) grid = c.num_tokens;
+    if (moe::launch_dispatch_pack_fp8(fp, static_cast<int>(grid), stages, ctx->pdl != 0, s) != cudaSuccess)
+      return MOE_ECUDA;
   }
   ctx->phase = kDispatched;
   return MOE_OK;

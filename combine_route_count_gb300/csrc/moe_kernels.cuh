@@ -102,6 +102,19 @@ size_t pack_bulk_smem_bytes(int stages, int piece_bytes);
 cudaError_t prepare_pack(int max_smem_bytes);  // one-time per-device attribute setup
 cudaError_t launch_dispatch_pack(const PackParams& p, const PackLaunch& l, cudaStream_t stream);
 
+// ---- dispatch_pack_fp8: block-scaled E4M3 payload ---------------------------
+struct PackFp8Params {
+  const uint8_t* x;         // bf16 [T, H]
+  uint8_t* expert_xq;       // e4m3 [rows, H]
+  float* expert_scales;     // [rows, H/128]
+  const int32_t* slot_row;  // [T*K]
+  int32_t* error_word;
+  int32_t T, K, H;          // H % 128 == 0
+};
+size_t pack_fp8_smem_bytes(int stages, int H);
+int pack_fp8_max_stages();
+cudaError_t launch_dispatch_pack_fp8(const PackFp8Params& p, int grid, int stages, bool pdl, cudaStream_t stream);
+
 // ---- combine: out[t] = bf16(sum_k w[t,k] * y[slot_row[t,k]]) -----------------
 struct CombineParams {
   const uint8_t* y;         // [rows, H] bf16

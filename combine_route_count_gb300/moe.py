@@ -36,7 +36,7 @@ PACK_BULK, PACK_VECTOR = 0, 1
 EXPORTS = ("moe_validate_config", "moe_workspace_bytes", "moe_recv_bound_rows", "moe_ctx_create",
            "moe_ctx_destroy", "moe_ctx_set_option", "moe_ctx_get_option", "moe_dispatch_send", "moe_dispatch_recv",
            "moe_combine_send", "moe_combine_recv", "moe_get_error", "moe_strerror",
-           "moe_dispatch_send_noalloc")
+           "moe_dispatch_send_noalloc", "moe_dispatch_send_fp8")
 
 
 class moe_config(ctypes.Structure):
@@ -80,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_ctx_set_option": ([P, I, I64], I),
         "moe_ctx_get_option": ([P, I, ctypes.POINTER(ctypes.c_int64)], I),
         "moe_dispatch_send": ([P, P, P, P, I64, P], I),
+        "moe_dispatch_send_fp8": ([P, P, P, P, P, I64, P], I),
         "moe_dispatch_recv": ([P, ctypes.POINTER(moe_dispatch_layout), P], I),
         "moe_combine_send": ([P, P, I64, P], I),
         "moe_combine_recv": ([P, P, P, P], I),
@@ -162,6 +163,15 @@ def moe_ctx_get_option(ctx: int, option: int) -> int:
 def moe_dispatch_send(ctx: int, x: Any, topk_idx: Any, expert_x: Any, expert_x_rows: int, stream: Any = None) -> None:
     _check(load_library().moe_dispatch_send(ctx, _ptr(x), _ptr(topk_idx), _ptr(expert_x), expert_x_rows,
                                             _stream(stream)), "moe_dispatch_send")
+
+
+MOE_FP8_BLOCK = 128
+
+
+def moe_dispatch_send_fp8(ctx: int, x: Any, topk_idx: Any, expert_xq: Any, expert_scales: Any, expert_rows: int,
+                          stream: Any = None) -> None:
+    _check(load_library().moe_dispatch_send_fp8(ctx, _ptr(x), _ptr(topk_idx), _ptr(expert_xq), _ptr(expert_scales),
+                                                expert_rows, _stream(stream)), "moe_dispatch_send_fp8")
 
 
 def moe_dispatch_recv(ctx: int, stream: Any = None) -> moe_dispatch_layout:
@@ -301,6 +311,10 @@ class MoELayer:
 
     def dispatch_send(self, x, topk_idx, expert_x, stream: Any = None) -> None:
         moe_dispatch_send(self.ctx, x, topk_idx, expert_x, expert_x.shape[0], stream)
+
+    def dispatch_send_fp8(self, x, topk_idx, expert_xq, expert_scales, stream: Any = None) -> None:
+        """fp8 payload: expert_xq uint8 [>= T*K, H], expert_scales float32 [>= T*K, H/128]."""
+        moe_dispatch_send_fp8(self.ctx, x, topk_idx, expert_xq, expert_scales, expert_xq.shape[0], stream)
 
     def dispatch_recv(self, stream: Any = None) -> "DispatchLayout":
         """The dispatch layout; its arrays are torch views into the workspace,

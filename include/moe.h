@@ -124,6 +124,27 @@ int moe_ctx_destroy(moe_ctx* ctx);
 int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_x,
                       int64_t expert_x_rows, void* stream);
 
+/* Dispatch, send half, with a block-scaled fp8 payload ("Efficient and
+ * portable mixture-of-experts communication", Dispatch: tokens are sent with
+ * their block scaling factors; "Enabling trillion-parameter models on AWS
+ * EFA", evaluation: block-scale fp8 dispatch, bf16 combine).  Same routing
+ * and row placement as moe_dispatch_send; each token row is quantised once:
+ * for every block of MOE_FP8_BLOCK consecutive elements,
+ *   scale = amax(|x|) / 448 in float32 (1 for an all-zero block),
+ *   inv = 1 / scale (float32 division, once per block),
+ *   q = E4M3(x * inv), float32 product, round to nearest even, saturating;
+ * and expert_xq[slot_row[t,k]] = q[t], expert_scales[slot_row[t,k]] = scale[t].
+ *   x              device bf16 [T, H], H % MOE_FP8_BLOCK == 0
+ *   expert_xq      device E4M3 bytes [expert_rows, H], 16-byte aligned
+ *   expert_scales  device float32 [expert_rows, H / MOE_FP8_BLOCK]
+ *   expert_rows    >= T*K; rows [0, T*K) of both are written
+ * The combine that follows still takes bf16 expert outputs.  Valid in the
+ * idle phase; MOE_EINVAL if H is not a multiple of the block or a bf16 row
+ * is too large for two shared-memory stages. */
+#define MOE_FP8_BLOCK 128
+int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_xq,
+                          float* expert_scales, int64_t expert_rows, void* stream);
+
 /* Dispatch, receive half.  On one GPU the send half already placed every row
  * in the grouped layout (the shared-buffer case of "Efficient and portable
  * mixture-of-experts communication", Further improvements), so this enqueues

@@ -46,7 +46,8 @@
 //    fp8 dispatch, bf16 combine).  The pages give neither the block nor the
 //    scale rule; read as blocks of 128 consecutive elements of a row, E4M3,
 //    scale = amax/448 so the largest element maps to the largest finite code,
-//    q = round-to-nearest-even(x / scale), saturating.
+//    and q = round-to-nearest-even(x * inv), saturating, with inv = 1/scale
+//    rounded once per block (the usual form: one multiply per element).
 //
 // All bf16 values are raw 16-bit patterns.
 
@@ -313,8 +314,8 @@ int oracle_combine_f64(int32_t T, int32_t H, int32_t K, const uint16_t* y, int64
 
 // Block-scaled fp8 quantisation of token rows (the dispatch payload with
 // "block scaling factors"): for each row and each block of 128 consecutive
-// elements, scale = amax / 448 (1 for an all-zero block), computed in float32,
-// and q = e4m3_rne_sat(x / scale) with a float32 division.
+// elements, scale = amax / 448 (1 for an all-zero block) and inv = 1 / scale,
+// both float32 divisions, and q = e4m3_rne_sat(x * inv) (float32 product).
 //   x       bf16 [T, H], H % 128 == 0
 //   q       e4m3 [T, H]
 //   scales  float32 [T, H/128]
@@ -327,9 +328,10 @@ int oracle_quantize_fp8(int32_t T, int32_t H, const uint16_t* x, uint8_t* q, flo
       float amax = 0.0f;
       for (int i = 0; i < kFp8Block; ++i) amax = std::max(amax, std::fabs(bf16_to_float(blk[i])));
       const float scale = amax > 0.0f ? amax / kE4m3Max : 1.0f;
+      const float inv = 1.0f / scale;
       scales[t * nb + b] = scale;
       for (int i = 0; i < kFp8Block; ++i)
-        q[t * H + static_cast<int64_t>(b) * kFp8Block + i] = float_to_e4m3_rne_sat(bf16_to_float(blk[i]) / scale);
+        q[t * H + static_cast<int64_t>(b) * kFp8Block + i] = float_to_e4m3_rne_sat(bf16_to_float(blk[i]) * inv);
     }
   }
   return ORACLE_OK;

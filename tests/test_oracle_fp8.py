@@ -5,8 +5,9 @@ The pages say dispatch carries tokens with block scaling factors
 the evaluated kernels use block-scale fp8 dispatch with bf16 combine
 ("Enabling trillion-parameter models on AWS EFA", evaluation); they do not
 give the block size or the scale rule.  The oracle reads them as blocks of
-128 consecutive elements, E4M3 codes, scale = amax / 448 and
-q = round-to-nearest-even(x / scale).  Pins:
+128 consecutive elements, E4M3 codes, scale = amax / 448, inv = 1 / scale
+(both float32 divisions, once per block) and q = round-to-nearest-even(x * inv).
+Pins:
 
 * the E4M3 rounding against torch's float32 -> float8_e4m3fn conversion (a
   library routine) inside the finite range, and the decoding of all 256 codes;
@@ -63,10 +64,10 @@ def test_e4m3_saturates_at_448(oracle_mod):
 
 
 def test_hand_worked_block(oracle_mod):
-    """Block [1, 2, -3, 0, 0, ...]: amax 3, scale 3/448;
-    1/scale = 149.33 -> nearest E4M3 144 = 1.125 * 2^7 -> code 0x71;
-    2/scale = 298.67 -> nearest 288 = 1.125 * 2^8 -> code 0x79;
-    -3/scale = -448 -> code 0xFE; zeros -> 0x00."""
+    """Block [1, 2, -3, 0, 0, ...]: amax 3, scale 3/448, inv = 1/scale ~ 149.33;
+    1*inv = 149.33 -> nearest E4M3 144 = 1.125 * 2^7 -> code 0x71;
+    2*inv = 298.67 -> nearest 288 = 1.125 * 2^8 -> code 0x79;
+    -3*inv = -448 (within rounding) -> code 0xFE; zeros -> 0x00."""
     x = np.zeros((1, 128), np.float32)
     x[0, :3] = [1.0, 2.0, -3.0]
     q, sc = oracle_mod.quantize_fp8(gen.to_bf16_bits(x))
