@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
         lib.oracle_double_to_bf16.restype = ctypes.c_uint16
         lib.oracle_fmaf.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float]
         lib.oracle_fmaf.restype = ctypes.c_float
+        lib.oracle_combine_two_level.argtypes = [i32, i32, i32, i32, i32, p, i64, p, p, p, p, p]
+        lib.oracle_combine_two_level.restype = ctypes.c_int
         lib.oracle_quantize_fp8.argtypes = [i32, i32, p, p, p]
         lib.oracle_quantize_fp8.restype = ctypes.c_int
         lib.oracle_float_to_e4m3.argtypes = [ctypes.c_float]
@@ -154,6 +156,33 @@ def combine_f64(y: np.ndarray, topk_w: np.ndarray, slot_row: np.ndarray):
     if rc != OK:
         raise OracleError(rc, "oracle_combine_f64")
     return out, exact, mag
+
+
+def combine_two_level(y: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, slot_row: np.ndarray,
+                      E: int, N: int, partial: Optional[np.ndarray] = None):
+    """Two-level combine with partial sums on the sending side (see
+    ``oracle_combine_two_level``).  Returns (out bf16 [T, H], partial bf16
+    [T*min(K,N), H], ranks_per_token int32 [T]); partial rows a token does not
+    use keep the values of the ``partial`` argument (zeros if None)."""
+    lib = _load()
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    sr = np.ascontiguousarray(slot_row, dtype=np.int32)
+    T, K = w.shape
+    H = y.shape[1]
+    slots = min(K, N)
+    part = np.zeros((T * slots, H), np.uint16) if partial is None else np.array(partial, dtype=np.uint16)
+    if part.shape != (T * slots, H):
+        raise ValueError("partial must be [T*min(K,N), H]")
+    out = np.zeros((T, H), dtype=np.uint16)
+    rc = lib.oracle_combine_two_level(T, H, K, E, N, _ptr(y), y.shape[0], _ptr(idx), _ptr(w), _ptr(sr),
+                                      _ptr(part), _ptr(out))
+    if rc != OK:
+        raise OracleError(rc, "oracle_combine_two_level")
+    L = E // N
+    ranks = np.array([len(set((idx[t] // L).tolist())) for t in range(T)], np.int32)
+    return out, part, ranks
 
 
 def float_to_bf16(f: float) -> int:

@@ -48,6 +48,15 @@
 //    scale = amax/448 so the largest element maps to the largest finite code,
 //    and q = round-to-nearest-even(x * inv), saturating, with inv = 1/scale
 //    rounded once per block (the usual form: one multiply per element).
+//  * Two-level combine with partial sums on the sending side ("Enabling
+//    trillion-parameter models on AWS EFA", evaluation, prefill: DeepEP sums a
+//    token's expert outputs on the sender to move less data, which can cost
+//    precision; the pages' own kernels sum only at the receiver).  Read as:
+//    on each rank r holding some of token t's experts, partial = bf16 of the
+//    same float32 fused-multiply-add chain restricted to those experts (top-k
+//    order, from +0.0); the token's rank then adds the float32 values of its
+//    partials in ascending r from +0.0 and rounds once to bf16.  Partial d of
+//    token t (d-th smallest rank) lives in row t*min(K,N) + d.
 //
 // All bf16 values are raw 16-bit patterns.
 
@@ -307,6 +316,52 @@ int oracle_combine_f64(int32_t T, int32_t H, int32_t K, const uint16_t* y, int64
       out[t * H + h] = double_to_bf16_rne(acc);
       if (exact) exact[t * H + h] = acc;
       if (abs_sum) abs_sum[t * H + h] = mag;
+    }
+  }
+  return ORACLE_OK;
+}
+
+// Two-level combine (partial sums on the sending side, then on the receiver):
+//   topk_idx  int32 [T, K] (the rank of slot k is topk_idx[t,k] / (E/N))
+//   partial   bf16 [T * min(K,N), H]: row t*min(K,N)+d holds the partial of the
+//             d-th smallest rank among token t's experts; rows past the
+//             token's number of ranks are left untouched
+//   out       bf16 [T, H]
+int oracle_combine_two_level(int32_t T, int32_t H, int32_t K, int32_t E, int32_t N, const uint16_t* y,
+                             int64_t y_rows, const int32_t* topk_idx, const float* topk_w,
+                             const int32_t* slot_row, uint16_t* partial, uint16_t* out) {
+  if (T < 0 || H < 1 || K < 1 || N < 1 || E < N || E % N != 0) return ORACLE_EINVAL;
+  for (int64_t p = 0; p < static_cast<int64_t>(T) * K; ++p) {
+    if (slot_row[p] < 0 || slot_row[p] >= y_rows) return ORACLE_EINVAL;
+    if (topk_idx[p] < 0 || topk_idx[p] >= E) return ORACLE_EROUTE;
+  }
+  const int32_t L = E / N;
+  const int32_t slots = std::min(K, N);
+  for (int64_t t = 0; t < T; ++t) {
+    // the ranks holding this token's experts, ascending, without repeats
+    std::vector<int32_t> ranks;
+    for (int32_t k = 0; k < K; ++k) ranks.push_back(topk_idx[t * K + k] / L);
+    std::sort(ranks.begin(), ranks.end());
+    ranks.erase(std::unique(ranks.begin(), ranks.end()), ranks.end());
+    // level 1: one partial per rank
+    for (size_t d = 0; d < ranks.size(); ++d) {
+      uint16_t* prow = partial + (t * slots + static_cast<int64_t>(d)) * H;
+      for (int64_t h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int32_t k = 0; k < K; ++k) {
+          if (topk_idx[t * K + k] / L != ranks[d]) continue;
+          int64_t row = slot_row[t * K + k];
+          acc = std::fmaf(topk_w[t * K + k], bf16_to_float(y[row * H + h]), acc);
+        }
+        prow[h] = float_to_bf16_rne(acc);
+      }
+    }
+    // level 2: the receiver adds the partials in rank order
+    for (int64_t h = 0; h < H; ++h) {
+      float acc = 0.0f;
+      for (size_t d = 0; d < ranks.size(); ++d)
+        acc = acc + bf16_to_float(partial[(t * slots + static_cast<int64_t>(d)) * H + h]);
+      out[t * H + h] = float_to_bf16_rne(acc);
     }
   }
   return ORACLE_OK;
