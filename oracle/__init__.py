@@ -64,6 +64,8 @@ def _load() -> ctypes.CDLL:
         lib.oracle_double_to_bf16.restype = ctypes.c_uint16
         lib.oracle_fmaf.argtypes = [ctypes.c_float, ctypes.c_float, ctypes.c_float]
         lib.oracle_fmaf.restype = ctypes.c_float
+        lib.oracle_dispatch_staged.argtypes = [i32, i32, i32, i32, i32, p, p, p, p, p, p]
+        lib.oracle_dispatch_staged.restype = ctypes.c_int
         lib.oracle_combine_two_level.argtypes = [i32, i32, i32, i32, i32, p, i64, p, p, p, p, p]
         lib.oracle_combine_two_level.restype = ctypes.c_int
         lib.oracle_quantize_fp8.argtypes = [i32, i32, p, p, p]
@@ -156,6 +158,25 @@ def combine_f64(y: np.ndarray, topk_w: np.ndarray, slot_row: np.ndarray):
     if rc != OK:
         raise OracleError(rc, "oracle_combine_f64")
     return out, exact, mag
+
+
+def dispatch_staged(x: np.ndarray, topk_idx: np.ndarray, E: int, N: int):
+    """Two-stage dispatch through per-peer send buffers (see
+    ``oracle_dispatch_staged``).  Returns (send_buf uint16 [T*K, H], send_dest
+    int32 [T*K], expert_x uint16 [T*K, H], slot_row int32 [T, K])."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, H = x.shape
+    K = idx.shape[1]
+    send = np.zeros((T * K, H), np.uint16)
+    dest = np.zeros(T * K, np.int32)
+    ex = np.zeros((T * K, H), np.uint16)
+    sr = np.zeros((T, K), np.int32)
+    rc = lib.oracle_dispatch_staged(T, H, K, E, N, _ptr(x), _ptr(idx), _ptr(send), _ptr(dest), _ptr(ex), _ptr(sr))
+    if rc != OK:
+        raise OracleError(rc, "oracle_dispatch_staged")
+    return send, dest, ex, sr
 
 
 def combine_two_level(y: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, slot_row: np.ndarray,

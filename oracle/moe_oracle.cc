@@ -57,6 +57,16 @@
 //    order, from +0.0); the token's rank then adds the float32 values of its
 //    partials in ascending r from +0.0 and rounds once to bf16.  Partial d of
 //    token t (d-th smallest rank) lives in row t*min(K,N) + d.
+//  * Two-stage dispatch through per-peer send buffers ("Enabling
+//    trillion-parameter models on AWS EFA", dispatch and combine timing: the
+//    sender copies tokens into contiguous per-peer send buffers at offsets
+//    from the cumulative sum of its per-expert counts; the receiver shuffles
+//    them from its receive buffer into the grouped-GEMM input).  Read as:
+//    source rank s's (token, slot) pairs, stably sorted by expert (which
+//    groups them by destination rank), fill send rows [s*T/N*K, (s+1)*T/N*K);
+//    the receiving side then copies each send row to its grouped row.  The
+//    result equals the direct placement; only the path (one more copy of every
+//    row) differs.
 //
 // All bf16 values are raw 16-bit patterns.
 
@@ -318,6 +328,47 @@ int oracle_combine_f64(int32_t T, int32_t H, int32_t K, const uint16_t* y, int64
       if (abs_sum) abs_sum[t * H + h] = mag;
     }
   }
+  return ORACLE_OK;
+}
+
+// Two-stage dispatch (per-peer send buffers, then the receiver's shuffle):
+//   send_buf   bf16 [T*K, H]: rows [s*T/N*K, (s+1)*T/N*K) hold source rank s's
+//              pairs in (expert, token, slot) order, each the token's x row
+//   send_dest  int32 [T*K]: the grouped row (slot_row) of each send row
+//   expert_x   bf16 [T*K, H]: expert_x[send_dest[j]] = send_buf[j]
+//   slot_row   int32 [T*K]: as oracle_dispatch (the grouped placement)
+int oracle_dispatch_staged(int32_t T, int32_t H, int32_t K, int32_t E, int32_t N, const uint16_t* x,
+                           const int32_t* topk_idx, uint16_t* send_buf, int32_t* send_dest, uint16_t* expert_x,
+                           int32_t* slot_row) {
+  int rc = check_sizes(T, H, K, E, N);
+  if (rc) return rc;
+  if (T > 0 && (!x || !topk_idx || !send_buf || !send_dest || !expert_x || !slot_row)) return ORACLE_EINVAL;
+  const int64_t rows = static_cast<int64_t>(T) * K;
+  // The grouped placement (slot_row) from the direct dispatch.
+  std::vector<uint16_t> direct(static_cast<size_t>(rows) * H);
+  std::vector<int32_t> counts(E), offsets(E + 1), src_off(static_cast<size_t>(E) * N), rank_off(N + 1),
+      row_src(static_cast<size_t>(rows));
+  rc = oracle_dispatch(T, H, K, E, N, x, topk_idx, direct.data(), rows, counts.data(), offsets.data(),
+                       src_off.data(), rank_off.data(), slot_row, row_src.data());
+  if (rc) return rc;
+  // Stage 1: each source rank fills its own send rows.
+  const int32_t Tr = T / N;
+  for (int32_t s = 0; s < N; ++s) {
+    std::vector<Triple> trip;
+    for (int32_t t = s * Tr; t < (s + 1) * Tr; ++t)
+      for (int32_t k = 0; k < K; ++k) trip.push_back({topk_idx[static_cast<int64_t>(t) * K + k], t, k});
+    std::stable_sort(trip.begin(), trip.end(), [](const Triple& a, const Triple& b) { return a.e < b.e; });
+    const int64_t base = static_cast<int64_t>(s) * Tr * K;
+    for (size_t j = 0; j < trip.size(); ++j) {
+      const Triple& p = trip[j];
+      std::memcpy(send_buf + (base + static_cast<int64_t>(j)) * H, x + static_cast<int64_t>(p.t) * H,
+                  sizeof(uint16_t) * H);
+      send_dest[base + static_cast<int64_t>(j)] = slot_row[static_cast<int64_t>(p.t) * K + p.k];
+    }
+  }
+  // Stage 2: the receivers move every send row to its grouped row.
+  for (int64_t j = 0; j < rows; ++j)
+    std::memcpy(expert_x + static_cast<int64_t>(send_dest[j]) * H, send_buf + j * H, sizeof(uint16_t) * H);
   return ORACLE_OK;
 }
 
