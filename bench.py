@@ -43,24 +43,44 @@ def parse():
     ap.add_argument("--buffer-sets", type=int, default=2)
     ap.add_argument("--payload", choices=["bf16", "fp8"], default="bf16",
                     help="dispatch payload: bf16 rows, or block-scaled fp8 rows (moe_dispatch_send_fp8)")
+    ap.add_argument("--dispatch", choices=["direct", "staged"], default="direct",
+                    help="rows straight to their grouped position (moe_dispatch_send), or through per-peer "
+                         "send buffers and a receive shuffle (moe_dispatch_send_staged)")
+    ap.add_argument("--combine", choices=["receiver", "two_level"], default="receiver",
+                    help="receiver-only combine (moe_combine_recv), or partial sums on the sending side "
+                         "then on the receiver (moe_combine_recv_two_level)")
+    ap.add_argument("--overlap", action="store_true",
+                    help="instead of the headline: how much of an independent GEMM (a shared-expert-sized "
+                         "bf16 matmul, random weights) the split send/receive layer hides, per MOE_OPT_MAX_SMS, "
+                         "and a two-micro-batch pipeline against the same work in sequence")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step per buffer set in a CUDA graph and replay it")
     return ap.parse_args()
 
 
-def algorithmic_bytes(w, payload="bf16"):
+def algorithmic_bytes(w, payload="bf16", partial_rows=None, staged=False):
     """Bytes a layer must move at minimum (see the design notes):
     dispatch reads x and writes T*K rows (bf16, or E4M3 bytes plus one float32
     scale per 128 elements); combine reads T*K bf16 rows and writes T rows;
-    plus the routing metadata."""
+    plus the routing metadata.  The two-level combine (partial_rows = the
+    number of (token, rank) partials) also writes and reads back its partial
+    rows.  The two-stage dispatch (staged) also writes every dispatched row
+    to its send buffer and reads it back."""
     T, H, K, E, N = w.T, w.H, w.K, w.E, w.N
     row = H * 2
     pairs = T * K
     out_row = row if payload == "bf16" else H + (H // 128) * 4
     dispatch = T * row + pairs * out_row
+    if staged:
+        dispatch += 2 * pairs * row
     dispatch_meta = 2 * pairs * 4 + 2 * pairs * 4 + pairs * 4 + (3 * E + E * N + N + 2) * 4
+    if staged:
+        dispatch_meta += 4 * pairs * 4
     combine = pairs * row + T * row
     combine_meta = pairs * 4 + pairs * 4
+    if partial_rows is not None:
+        combine += 2 * partial_rows * row
+        combine_meta += pairs * 4 + (N + 1) * 4
     return {"dispatch": dispatch + dispatch_meta, "combine": combine + combine_meta,
             "total": dispatch + dispatch_meta + combine + combine_meta}
 
@@ -246,22 +266,37 @@ def run_gpu(args):
                              if args.payload == "bf16" else torch.empty((rows, H), dtype=torch.uint8, device=dev),
                              expert_scales=None if args.payload == "bf16"
                              else torch.empty((rows, H // 128), dtype=torch.float32, device=dev),
-                             out=torch.empty((T, H), dtype=torch.int16, device=dev)))
+                             out=torch.empty((T, H), dtype=torch.int16, device=dev),
+                             partial=torch.empty((T * min(K, N), H), dtype=torch.int16, device=dev)
+                             if args.combine == "two_level" else None,
+                             send=torch.empty((rows, H), dtype=torch.int16, device=dev)
+                             if args.dispatch == "staged" else None))
         del x0, idx0, w0, y0
     torch.cuda.synchronize(dev)
     layer = moe.MoELayer(T, H, K, E, N, device=dev)
 
+    if args.dispatch == "staged" and args.payload != "bf16":
+        raise SystemExit("--dispatch staged moves bf16 rows only")
+
     def dispatch(s):
-        if args.payload == "bf16":
+        if args.dispatch == "staged":
+            layer.dispatch_send_staged(s["x"], s["idx"], s["send"], s["expert_x"], stream)
+        elif args.payload == "bf16":
             layer.dispatch_send(s["x"], s["idx"], s["expert_x"], stream)
         else:
             layer.dispatch_send_fp8(s["x"], s["idx"], s["expert_x"], s["expert_scales"], stream)
+
+    def combine(s):
+        if args.combine == "receiver":
+            layer.combine_recv(s["w"], s["out"], stream)
+        else:
+            layer.combine_recv_two_level(s["w"], s["partial"], s["out"], stream)
 
     def step(s):
         dispatch(s)
         layer.dispatch_recv(stream)
         layer.combine_send(s["y"], stream)
-        layer.combine_recv(s["w"], s["out"], stream)
+        combine(s)
 
     def barrier():
         if ws > 1:
@@ -334,37 +369,47 @@ def run_gpu(args):
         ev[i][1].record(stream)
         layer.dispatch_recv(stream)
         layer.combine_send(s["y"], stream)
-        layer.combine_recv(s["w"], s["out"], stream)
+        combine(s)
         ev[i][2].record(stream)
     torch.cuda.synchronize(dev)
     layer_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(n_attr)]
     disp_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n_attr)]
     comb_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n_attr)]
 
-    ab = algorithmic_bytes(w, args.payload)
+    partial_rows = None
+    if args.combine == "two_level":
+        ranks = np.sort(li.topk_idx // (E // N), axis=1)
+        partial_rows = int(T + np.count_nonzero(np.diff(ranks, axis=1)))  # distinct ranks per token, summed
+    ab = algorithmic_bytes(w, args.payload, partial_rows, args.dispatch == "staged")
     peak, peak_kind = measured_peaks()
     disp_us = statistics.mean(disp_ms) * 1e3
     comb_us = statistics.mean(comb_ms) * 1e3
     kernels = {
         "dispatch_send": {"us": round(disp_us, 2), "bytes": ab["dispatch"],
                           "gbs": round(ab["dispatch"] / disp_us / 1e3, 1),
-                          "kernels": ["route_cluster", "dispatch_pack"]},
+                          "kernels": ["route_cluster", "dispatch_pack"] if args.dispatch == "direct"
+                          else ["route_cluster", "staged_layout", "dispatch_pack (send rows)",
+                                "dispatch_pack (receive shuffle)"]},
         "combine_recv": {"us": round(comb_us, 2), "bytes": ab["combine"],
-                         "gbs": round(ab["combine"] / comb_us / 1e3, 1), "kernels": ["combine"]},
+                         "gbs": round(ab["combine"] / comb_us / 1e3, 1),
+                         "kernels": ["combine"] if args.combine == "receiver"
+                         else ["combine_partial", "combine_reduce"]},
         "attribution": f"separate pass of {n_attr} steps with an event between the phases "
                        f"(layer {statistics.mean(layer_ms) * 1e3:.1f} us there)",
     }
     if comb_us >= disp_us:
-        dom, dom_us, dom_bytes, dom_kernel = "combine", comb_us, ab["combine"], "combine"
+        dom, dom_us, dom_bytes = "combine", comb_us, ab["combine"]
+        dom_kernel = "combine" if args.combine == "receiver" else "combine_two_level"
     else:
-        dom, dom_us, dom_bytes, dom_kernel = "route+dispatch_pack", disp_us, ab["dispatch"], "dispatch_pack"
+        dom, dom_us, dom_bytes = "route+dispatch_pack", disp_us, ab["dispatch"]
+        dom_kernel = "dispatch_pack" if args.dispatch == "direct" else "dispatch_staged"
     achieved = dom_bytes / dom_us / 1e3
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": committed_traffic(dom_kernel, w.name),
                 "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"}
 
     e2e = None
-    if not args.no_e2e and args.payload == "bf16":
+    if not args.no_e2e and args.payload == "bf16" and args.combine == "receiver" and args.dispatch == "direct":
         e2e = run_e2e(args, w, li, layer, stream, dev)
 
     cpu = None
@@ -383,11 +428,15 @@ def run_gpu(args):
                              f"{args.buffer_sets} rotating buffer sets",
                        "launch": "CUDA graph replay" if args.graph else "direct C-ABI calls",
                        "payload": args.payload,
+                       "dispatch": "direct placement" if args.dispatch == "direct"
+                                   else "two-stage: per-peer send rows, then receive shuffle",
                        "pack": f"bulk (TMA), {layer.get_option(moe.MOE_OPT_PACK_STAGES) or 'auto'} stages, "
                                f"prefetch={layer.get_option(moe.MOE_OPT_PACK_PREFETCH)}, "
                                f"hints={layer.get_option(moe.MOE_OPT_CACHE_HINTS)}, PDL",
-                       "combine": "bulk (TMA gather)" if layer.get_option(moe.MOE_OPT_COMBINE_VARIANT) == 0
-                                  else "vector",
+                       "combine": ("two-level: sending-side partial sums, "
+                                   f"{partial_rows} partial rows" if args.combine == "two_level"
+                                   else "bulk (TMA gather)" if layer.get_option(moe.MOE_OPT_COMBINE_VARIANT) == 0
+                                   else "vector"),
                        "routing": {1: "route_count (1 block)", 2: "route_local+route_finalize",
                                    3: f"route_cluster ({layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS)} CTAs)"}[
                            layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)]},
@@ -399,7 +448,8 @@ def run_gpu(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clk,
-            "gpu_launches": layer.kernels_per_layer() * args.steps,
+            "gpu_launches": (layer.kernels_per_layer() + (args.combine == "two_level")
+                             + 2 * (args.dispatch == "staged")) * args.steps,
         }
         print(json.dumps(line), flush=True)
     layer.close()
@@ -484,10 +534,159 @@ def run_e2e(args, w, li, layer, stream, dev):
             "steps": steps, "pipelined": True, "out_matches_device": ok}
 
 
+def run_overlap(args):
+    """Split send/receive halves let other work run between and beside them
+    ("Efficient and portable mixture-of-experts communication", Benchmarks:
+    splitting into send and receive parts can hide latency; "Enabling
+    trillion-parameter models on AWS EFA", evaluation: micro-batching).  On one
+    GPU the layer is HBM-bound and a bf16 GEMM is tensor-bound, so they can
+    share the SMs.  Measured here, each over `steps` iterations between events:
+      layer      dispatch_send..combine_recv alone;
+      gemm       the independent work alone: [T, H] x [H, 4096] bf16 (the
+                 gate+up projection of a DeepSeek-sized shared expert);
+      serial     layer then gemm on one stream;
+      overlap    layer on one stream, gemm on another, joined each step, for
+                 several MOE_OPT_MAX_SMS values;
+      pipeline   two micro-batches of T/2 tokens (two contexts): each
+                 micro-batch's GEMM (on the T/2 tokens) runs on a second
+                 stream between its dispatch and its combine, so micro-batch
+                 1's dispatch overlaps micro-batch 0's GEMM; against the same
+                 calls in sequence on one stream."""
+    import numpy as np
+    import torch
+
+    from combine_route_count_gb300 import build as build_mod
+    from combine_route_count_gb300 import inputs as gen
+    from combine_route_count_gb300 import moe
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build_mod.build()
+    moe.load_library()
+    w = gen.BY_NAME[args.workload]
+    li = gen.make_inputs(w)
+    T, H, K, E, N = w.T, w.H, w.K, w.E, w.N
+    steps = max(10, min(args.steps, 200))
+    sa, sb = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    x = torch.from_numpy(li.x.view(np.int16)).to(dev)
+    idx = torch.from_numpy(li.topk_idx).to(dev)
+    wts = torch.from_numpy(li.topk_w).to(dev)
+    y = torch.from_numpy(li.y.view(np.int16)).to(dev)
+    ex = torch.empty((T * K, H), dtype=torch.int16, device=dev)
+    out = torch.empty((T, H), dtype=torch.int16, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    a_mat = torch.randn((T, H), generator=g, device=dev, dtype=torch.bfloat16)
+    b_mat = torch.randn((H, 4096), generator=g, device=dev, dtype=torch.bfloat16) * (H ** -0.5)
+    c_mat = torch.empty((T, 4096), device=dev, dtype=torch.bfloat16)
+    layer = moe.MoELayer(T, H, K, E, N, device=dev)
+
+    def run_layer(lay, s, xx, ii, ww, yy, ee, oo):
+        lay.dispatch_send(xx, ii, ee, s)
+        lay.dispatch_recv(s)
+        lay.combine_send(yy, s)
+        lay.combine_recv(ww, oo, s)
+
+    def gemm(s, a=a_mat, c=c_mat):
+        with torch.cuda.stream(s):
+            torch.matmul(a, b_mat, out=c)
+
+    def timed(fn, stream):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps * 1e3
+
+    def fork_join(body_a, body_b):
+        ev0, ev1 = torch.cuda.Event(), torch.cuda.Event()
+        ev0.record(sa)
+        sb.wait_event(ev0)
+        body_a()
+        body_b()
+        ev1.record(sb)
+        sa.wait_event(ev1)
+
+    t_layer = timed(lambda: run_layer(layer, sa, x, idx, wts, y, ex, out), sa)
+    t_gemm = timed(lambda: gemm(sa), sa)
+    t_serial = timed(lambda: (run_layer(layer, sa, x, idx, wts, y, ex, out), gemm(sa)), sa)
+    overlap = []
+    for max_sms in (0, 128, 112, 96, 76):
+        layer.set_option(moe.MOE_OPT_MAX_SMS, max_sms)
+        t_l = timed(lambda: run_layer(layer, sa, x, idx, wts, y, ex, out), sa)
+        t_o = timed(lambda: fork_join(lambda: run_layer(layer, sa, x, idx, wts, y, ex, out), lambda: gemm(sb)), sa)
+        overlap.append({"max_sms": max_sms, "layer_alone_us": round(t_l, 2), "overlap_us": round(t_o, 2),
+                        "hidden_frac": round((t_l + t_gemm - t_o) / min(t_l, t_gemm), 3)})
+    layer.set_option(moe.MOE_OPT_MAX_SMS, 0)
+    if layer.get_error(sa) != moe.MOE_OK:
+        raise RuntimeError("device reported an error in the overlap pass")
+
+    # Two micro-batches of T/2 tokens.
+    Th = T // 2
+    mbs = []
+    for m in range(2):
+        sl = slice(m * Th, (m + 1) * Th)
+        lm = moe.MoELayer(Th, H, K, E, N, device=dev)
+        mbs.append(dict(layer=lm, x=x[sl].contiguous(), idx=idx[sl].contiguous(), w=wts[sl].contiguous(),
+                        y=y[: Th * K].contiguous(), ex=torch.empty((Th * K, H), dtype=torch.int16, device=dev),
+                        out=torch.empty((Th, H), dtype=torch.int16, device=dev), a=a_mat[sl],
+                        c=torch.empty((Th, 4096), device=dev, dtype=torch.bfloat16)))
+
+    def mb_sequential():
+        for mb in mbs:
+            mb["layer"].dispatch_send(mb["x"], mb["idx"], mb["ex"], sa)
+            mb["layer"].dispatch_recv(sa)
+            gemm(sa, mb["a"], mb["c"])
+            mb["layer"].combine_send(mb["y"], sa)
+            mb["layer"].combine_recv(mb["w"], mb["out"], sa)
+
+    def mb_pipelined():
+        start = torch.cuda.Event()
+        start.record(sa)
+        sb.wait_event(start)
+        done = []
+        for mb in mbs:
+            mb["layer"].dispatch_send(mb["x"], mb["idx"], mb["ex"], sa)
+            mb["layer"].dispatch_recv(sa)
+            ev = torch.cuda.Event()
+            ev.record(sa)
+            sb.wait_event(ev)  # this micro-batch's GEMM needs its dispatched rows
+            gemm(sb, mb["a"], mb["c"])
+            e2 = torch.cuda.Event()
+            e2.record(sb)
+            done.append(e2)
+        for mb, e2 in zip(mbs, done):
+            sa.wait_event(e2)
+            mb["layer"].combine_send(mb["y"], sa)
+            mb["layer"].combine_recv(mb["w"], mb["out"], sa)
+
+    t_mb_seq = timed(mb_sequential, sa)
+    t_mb_pipe = timed(mb_pipelined, sa)
+    for mb in mbs:
+        if mb["layer"].get_error(sa) != moe.MOE_OK:
+            raise RuntimeError("device reported an error in the micro-batch pass")
+        mb["layer"].close()
+    layer.close()
+    line = {"metric": "overlap of the split dispatch/combine with an independent bf16 GEMM", "unit": "us",
+            "workload": w.name, "steps": steps, "layer_us": round(t_layer, 2), "gemm_us": round(t_gemm, 2),
+            "gemm": f"[{T}, {H}] x [{H}, 4096] bf16 torch.matmul on a second stream", "serial_us": round(t_serial, 2),
+            "overlap": overlap,
+            "micro_batches": {"sequential_us": round(t_mb_seq, 2), "pipelined_us": round(t_mb_pipe, 2),
+                              "tokens_per_micro_batch": Th, "gemm_per_micro_batch": f"[{Th}, {H}] x [{H}, 4096]"}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.overlap:
+        run_overlap(args)
     else:
         run_gpu(args)
 

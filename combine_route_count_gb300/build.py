@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ["route_count.cu", "route_split.cu", "route_cluster.cu", "dispatch_pack.cu", "dispatch_fp8.cu", "combine.cu", "moe_abi.cu", "moe_noalloc.cu"]
+SOURCES = ["route_count.cu", "route_split.cu", "route_cluster.cu", "dispatch_pack.cu", "dispatch_fp8.cu", "dispatch_staged.cu", "combine.cu", "combine_two_level.cu", "moe_abi.cu", "moe_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -138,12 +138,21 @@ __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stage
 
   int64_t i = 0;
   bool ok = true;
+  // Destination rows are loaded one unit ahead, so that their latency is not
+  // on the path of every unit (it matters when a unit has few stores).
+  // Coherent loads: the table is written by the previous grid.
+  auto dest_row = [&](int64_t unit_index) -> int {
+    const int64_t tt = (first + unit_index * step) / p.pieces;
+    return lane < p.K ? p.slot_row[tt * p.K + lane] : -1;
+  };
+  int next_row = mine > 0 ? dest_row(0) : -1;
   for (; i < mine; ++i) {
     const int64_t u = first + i * step;
     const int64_t t = u / p.pieces;
     const int j = static_cast<int>(u - t * p.pieces);
     const int s = static_cast<int>(i % stages);
-    const int row = lane < p.K ? p.slot_row[t * p.K + lane] : -1;  // coherent load: written by the previous grid
+    const int row = next_row;
+    if (i + 1 < mine) next_row = dest_row(i + 1);
     // Every lane waits; the outcome is made warp-uniform so that no lane is
     // left behind at a later __syncwarp.
     const bool arrived = wait_phase(&bars[s], static_cast<uint32_t>((i / stages) & 1));

@@ -60,7 +60,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct WorkspaceLayout {
   size_t error_word, expert_counts, expert_offsets, src_offsets, rank_offsets, slot_row, row_src, hist, block_err,
-      total;
+      send_pos, send_dest, plan_row, plan_w, plan_mask, total;
 };
 
 WorkspaceLayout layout_of(const moe_config& c) {
@@ -85,6 +85,16 @@ WorkspaceLayout layout_of(const moe_config& c) {
   o += align_up(sizeof(int32_t) * static_cast<size_t>(moe::kMaxSplitBlocks) * c.num_experts);
   l.block_err = o;
   o += align_up(sizeof(int32_t) * moe::kMaxSplitBlocks);
+  l.send_pos = o;  // two-stage dispatch: send row of each (token, slot) pair
+  o += align_up(sizeof(int32_t) * pairs);
+  l.send_dest = o;  // two-stage dispatch: grouped row of each send row
+  o += align_up(sizeof(int32_t) * pairs);
+  l.plan_row = o;  // two-level combine: sorted slots, weights, group ends
+  o += align_up(sizeof(int32_t) * pairs);
+  l.plan_w = o;
+  o += align_up(sizeof(float) * pairs);
+  l.plan_mask = o;
+  o += align_up(sizeof(int32_t) * static_cast<size_t>(c.num_tokens));
   l.total = o;
   return l;
 }
@@ -99,6 +109,7 @@ struct moe_ctx {
   size_t ws_bytes;
   int device;
   int num_sms;
+  int max_sms;  // MOE_OPT_MAX_SMS: 0 = every SM
   int max_smem_optin;
   int l2_bytes;
   int phase;
@@ -113,6 +124,11 @@ struct moe_ctx {
   int32_t* row_src;
   int32_t* hist;
   int32_t* block_err;
+  int32_t* send_pos;
+  int32_t* send_dest;
+  int32_t* plan_row;
+  float* plan_w;
+  int32_t* plan_mask;
   // launch options (MOE_OPT_* in moe.h)
   int pack_variant;
   int pack_stages;
@@ -202,6 +218,11 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->row_src = reinterpret_cast<int32_t*>(c->ws + l.row_src);
   c->hist = reinterpret_cast<int32_t*>(c->ws + l.hist);
   c->block_err = reinterpret_cast<int32_t*>(c->ws + l.block_err);
+  c->send_pos = reinterpret_cast<int32_t*>(c->ws + l.send_pos);
+  c->send_dest = reinterpret_cast<int32_t*>(c->ws + l.send_dest);
+  c->plan_row = reinterpret_cast<int32_t*>(c->ws + l.plan_row);
+  c->plan_w = reinterpret_cast<float*>(c->ws + l.plan_w);
+  c->plan_mask = reinterpret_cast<int32_t*>(c->ws + l.plan_mask);
   c->pack_variant = moe::kPackBulk;
   c->pack_stages = 0;  // automatic: about 100 KiB of stages per CTA
   c->pack_prefetch = 2;
@@ -253,7 +274,11 @@ int combine_variant_of(const moe_ctx* c) {
   if (c->combine_variant >= 0) return c->combine_variant;
   return c->cfg.top_k >= 4 ? moe::kCombineBulk : moe::kCombineVector;
 }
-int pack_ctas_auto(const moe_ctx* c) { return c->cfg.top_k >= 4 ? 2 : 3; }
+// Bulk pack CTAs per SM: 2 when a token row has K >= 4 destinations, else 3.
+int pack_ctas_auto(int K) { return K >= 4 ? 2 : 3; }
+
+// SMs the persistent grids may spread over (MOE_OPT_MAX_SMS).
+int grid_sms(const moe_ctx* c) { return c->max_sms > 0 && c->max_sms < c->num_sms ? c->max_sms : c->num_sms; }
 
 }  // namespace
 
@@ -307,6 +332,10 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
     case MOE_OPT_COMBINE_CTAS_PER_SM:
       if (value < 0 || value > 32) return MOE_EINVAL;
       ctx->combine_ctas_per_sm = static_cast<int>(value);
+      return MOE_OK;
+    case MOE_OPT_MAX_SMS:
+      if (value < 0 || value > ctx->num_sms) return MOE_EINVAL;
+      ctx->max_sms = static_cast<int>(value);
       return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       if (value < 0 || value > 3) return MOE_EINVAL;
@@ -363,6 +392,9 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
     case MOE_OPT_COMBINE_CTAS_PER_SM:
       *value = ctx->combine_ctas_per_sm;
       return MOE_OK;
+    case MOE_OPT_MAX_SMS:
+      *value = ctx->max_sms;
+      return MOE_OK;
     default:
       return MOE_EINVAL;
   }
@@ -385,7 +417,7 @@ int pack_piece_bytes(const moe_ctx* c, int64_t row_bytes) {
 int pack_grid(const moe_ctx* c, const moe::PackParams& p, int stages) {
   const bool bulk = c->pack_variant == moe::kPackBulk;
   const int64_t units = static_cast<int64_t>(p.T) * p.pieces;
-  int per_sm = c->pack_ctas_per_sm > 0 ? c->pack_ctas_per_sm : (bulk ? pack_ctas_auto(c) : 0);
+  int per_sm = c->pack_ctas_per_sm > 0 ? c->pack_ctas_per_sm : (bulk ? pack_ctas_auto(p.K) : 0);
   if (bulk) {
     const size_t smem = moe::pack_bulk_smem_bytes(stages, p.piece_bytes);
     // 228 KiB of shared memory per SM, 1 KiB of it reserved per resident CTA.
@@ -395,7 +427,7 @@ int pack_grid(const moe_ctx* c, const moe::PackParams& p, int stages) {
   } else if (per_sm <= 0) {
     per_sm = 8;  // 8 x 256 threads
   }
-  int64_t grid = static_cast<int64_t>(c->num_sms) * per_sm;
+  int64_t grid = static_cast<int64_t>(grid_sms(c)) * per_sm;
   const int64_t useful = bulk ? units : (units + 7) / 8;
   if (grid > useful) grid = useful;
   if (grid < 1) grid = 1;
@@ -472,6 +504,75 @@ int enqueue_routing(moe_ctx* ctx, const int32_t* topk_idx, cudaStream_t s) {
 
 }  // namespace
 
+namespace {
+
+// Enqueues the pack kernel of the context's variant: dst[table[t*K+k]] = src[t]
+// for T source rows of H bf16 each (a table entry < 0 is skipped).  The
+// bulk pack reads its first source rows before waiting on the previous
+// kernel, so `pdl` must be false when src is that kernel's output.
+// `prefetch` allows the context's L2 prefetch of source rows (which pays
+// while the pack overlaps routing).
+int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, const int32_t* table, int32_t T, int32_t K,
+                 bool pdl, bool prefetch, cudaStream_t s) {
+  moe::PackParams pp = {};
+  pp.x = static_cast<const uint8_t*>(src);
+  pp.expert_x = static_cast<uint8_t*>(dst);
+  pp.slot_row = table;
+  pp.error_word = ctx->error_word;
+  pp.T = T;
+  pp.K = K;
+  pp.row_bytes = static_cast<int64_t>(ctx->cfg.hidden) * 2;
+  pp.piece_bytes = pack_piece_bytes(ctx, pp.row_bytes);
+  pp.pieces = static_cast<int32_t>((pp.row_bytes + pp.piece_bytes - 1) / pp.piece_bytes);
+  moe::PackLaunch pl = {};
+  pl.variant = ctx->pack_variant;
+  pl.stages = ctx->pack_stages;
+  if (pl.stages <= 0) {
+    // About 100 KiB of stages per CTA (two CTAs per SM), 2..16 stages.
+    pl.stages = static_cast<int>((200 * 1024) / pack_ctas_auto(K) / pp.piece_bytes);
+    if (pl.stages > 16) pl.stages = 16;
+    if (pl.stages < 2) pl.stages = 2;
+  }
+  if (pl.variant == moe::kPackBulk) {
+    // Shrink the pipeline if the stages do not fit in one CTA's shared memory.
+    while (pl.stages > 2 &&
+           moe::pack_bulk_smem_bytes(pl.stages, pp.piece_bytes) > static_cast<size_t>(ctx->max_smem_optin))
+      --pl.stages;
+    if (moe::pack_bulk_smem_bytes(pl.stages, pp.piece_bytes) > static_cast<size_t>(ctx->max_smem_optin))
+      return MOE_EINVAL;
+  }
+  pl.grid = pack_grid(ctx, pp, pl.stages);
+  pl.prefetch = prefetch ? ctx->pack_prefetch : 0;
+  pl.prefetch_units = -1;
+  if (pl.prefetch == 2) {
+    // Evict-last prefetch when every row a CTA still needs after its
+    // prologue fits, across the grid, in a third of L2.  (Measured on
+    // GB300: it pays at DeepSeek size even beyond the device's persisting
+    // L2 carve-out, so that carve-out does not bound it.)
+    const int64_t budget = static_cast<int64_t>(ctx->l2_bytes) / 3;
+    const int64_t units = static_cast<int64_t>(pp.T) * pp.pieces;
+    const int64_t per_cta = (units + pl.grid - 1) / pl.grid - pl.stages;  // units past the prologue
+    const int64_t fit = budget > 0 ? budget / (static_cast<int64_t>(pl.grid) * pp.piece_bytes) : 0;
+    if (per_cta > 0 && fit >= per_cta) {
+      pl.prefetch_units = static_cast<int>(per_cta);
+    } else {
+      // The token rows do not fit: marking part of them evict-last was
+      // measured slower (Kimi-sized layers) than prefetching all normally.
+      pl.prefetch = 1;
+    }
+  }
+  pl.pdl = pdl;
+  pl.hints = ctx->cache_hints;
+  // Two store groups in flight by default (measured on GB300 with the
+  // destination rows loaded one unit ahead: DeepSeek-, worst-case- and
+  // Mixtral-sized layers and the two-stage dispatch gain over one).
+  pl.depth = ctx->pack_depth > 0 ? ctx->pack_depth : 2;
+  if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
 MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_x,
                               int64_t expert_x_rows, void* stream) {
   if (!ctx) return MOE_EINVAL;
@@ -488,57 +589,49 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
   if (rrc != MOE_OK) return rrc;
 
   if (c.num_tokens > 0) {
-    moe::PackParams pp = {};
-    pp.x = static_cast<const uint8_t*>(x);
-    pp.expert_x = static_cast<uint8_t*>(expert_x);
-    pp.slot_row = ctx->slot_row;
-    pp.error_word = ctx->error_word;
-    pp.T = c.num_tokens;
-    pp.K = c.top_k;
-    pp.row_bytes = static_cast<int64_t>(c.hidden) * 2;
-    pp.piece_bytes = pack_piece_bytes(ctx, pp.row_bytes);
-    pp.pieces = static_cast<int32_t>((pp.row_bytes + pp.piece_bytes - 1) / pp.piece_bytes);
-    moe::PackLaunch pl = {};
-    pl.variant = ctx->pack_variant;
-    pl.stages = ctx->pack_stages;
-    if (pl.stages <= 0) {
-      // About 100 KiB of stages per CTA (two CTAs per SM), 2..16 stages.
-      pl.stages = static_cast<int>((200 * 1024) / pack_ctas_auto(ctx) / pp.piece_bytes);
-      if (pl.stages > 16) pl.stages = 16;
-      if (pl.stages < 2) pl.stages = 2;
-    }
-    if (pl.variant == moe::kPackBulk) {
-      // Shrink the pipeline if the stages do not fit in one CTA's shared memory.
-      while (pl.stages > 2 &&
-             moe::pack_bulk_smem_bytes(pl.stages, pp.piece_bytes) > static_cast<size_t>(ctx->max_smem_optin))
-        --pl.stages;
-      if (moe::pack_bulk_smem_bytes(pl.stages, pp.piece_bytes) > static_cast<size_t>(ctx->max_smem_optin))
-        return MOE_EINVAL;
-    }
-    pl.grid = pack_grid(ctx, pp, pl.stages);
-    pl.prefetch = ctx->pack_prefetch;
-    pl.prefetch_units = -1;
-    if (pl.prefetch == 2) {
-      // Evict-last prefetch when every row a CTA still needs after its
-      // prologue fits, across the grid, in a third of L2.  (Measured on
-      // GB300: it pays at DeepSeek size even beyond the device's persisting
-      // L2 carve-out, so that carve-out does not bound it.)
-      const int64_t budget = static_cast<int64_t>(ctx->l2_bytes) / 3;
-      const int64_t units = static_cast<int64_t>(pp.T) * pp.pieces;
-      const int64_t per_cta = (units + pl.grid - 1) / pl.grid - pl.stages;  // units past the prologue
-      const int64_t fit = budget > 0 ? budget / (static_cast<int64_t>(pl.grid) * pp.piece_bytes) : 0;
-      if (per_cta > 0 && fit >= per_cta) {
-        pl.prefetch_units = static_cast<int>(per_cta);
-      } else {
-        // The token rows do not fit: marking part of them evict-last was
-        // measured slower (Kimi-sized layers) than prefetching all normally.
-        pl.prefetch = 1;
-      }
-    }
-    pl.pdl = ctx->pdl != 0;
-    pl.hints = ctx->cache_hints;
-    pl.depth = ctx->pack_depth;
-    if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
+    const int prc = enqueue_pack(ctx, x, expert_x, ctx->slot_row, c.num_tokens, c.top_k, ctx->pdl != 0, true, s);
+    if (prc != MOE_OK) return prc;
+  }
+  ctx->phase = kDispatched;
+  return MOE_OK;
+}
+
+MOE_API int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* send_buf,
+                                     int64_t send_rows, void* expert_x, int64_t expert_x_rows, void* stream) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->phase != kIdle) return MOE_ESTATE;
+  const moe_config& c = ctx->cfg;
+  const int64_t pairs = static_cast<int64_t>(c.num_tokens) * c.top_k;
+  if (expert_x_rows < pairs || send_rows < pairs) return MOE_EINVAL;
+  if (c.num_tokens > 0) {
+    if (!x || !topk_idx || !send_buf || !expert_x) return MOE_EINVAL;
+    if (!aligned(x, 16) || !aligned(send_buf, 16) || !aligned(expert_x, 16) || !aligned(topk_idx, 4))
+      return MOE_EINVAL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rrc = enqueue_routing(ctx, topk_idx, s);
+  if (rrc != MOE_OK) return rrc;
+  if (c.num_tokens > 0) {
+    moe::StagedLayoutParams sp = {};
+    sp.topk_idx = topk_idx;
+    sp.slot_row = ctx->slot_row;
+    sp.expert_offsets = ctx->expert_offsets;
+    sp.src_offsets = ctx->src_offsets;
+    sp.send_pos = ctx->send_pos;
+    sp.send_dest = ctx->send_dest;
+    sp.T = c.num_tokens;
+    sp.K = c.top_k;
+    sp.E = c.num_experts;
+    sp.N = c.num_ranks;
+    if (moe::launch_staged_layout(sp, ctx->pdl != 0, s) != cudaSuccess) return MOE_ECUDA;
+    // Stage 1, every source rank: x rows into its per-peer send rows.
+    int prc = enqueue_pack(ctx, x, send_buf, ctx->send_pos, c.num_tokens, c.top_k, ctx->pdl != 0, true, s);
+    if (prc != MOE_OK) return prc;
+    // Stage 2, every receiver: send rows into the grouped rows.  Its source is
+    // the previous kernel's output, so it is not launched early, and there is
+    // nothing for an L2 prefetch to overlap.
+    prc = enqueue_pack(ctx, send_buf, expert_x, ctx->send_dest, static_cast<int32_t>(pairs), 1, false, false, s);
+    if (prc != MOE_OK) return prc;
   }
   ctx->phase = kDispatched;
   return MOE_OK;
@@ -585,7 +678,7 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
     const int want = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : 3;
     if (per_sm > want) per_sm = want;
     if (per_sm < 1) per_sm = 1;
-    int64_t grid = static_cast<int64_t>(ctx->num_sms) * per_sm;
+    int64_t grid = static_cast<int64_t>(grid_sms(ctx)) * per_sm;
     if (grid > c.num_tokens) grid = c.num_tokens;
     if (moe::launch_dispatch_pack_fp8(fp, static_cast<int>(grid), stages, ctx->pdl != 0, s) != cudaSuccess)
       return MOE_ECUDA;
@@ -655,11 +748,53 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
       int per_sm = ctx->combine_ctas_per_sm > 0 && ctx->combine_ctas_per_sm < fit ? ctx->combine_ctas_per_sm : fit;
       if (per_sm < 1) per_sm = 1;
       const int64_t units = static_cast<int64_t>(c.num_tokens) * cl.shape.pieces;
-      int64_t grid = static_cast<int64_t>(ctx->num_sms) * per_sm;
+      int64_t grid = static_cast<int64_t>(grid_sms(ctx)) * per_sm;
       if (grid > units) grid = units;
       cl.grid = static_cast<int>(grid);
     }
     if (moe::launch_combine(cp, cl, static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ECUDA;
+  }
+  ctx->expert_y = nullptr;
+  ctx->phase = kIdle;
+  return MOE_OK;
+}
+
+MOE_API int moe_partial_rows(const moe_config* cfg, int64_t* rows) {
+  if (!cfg || !rows) return MOE_EINVAL;
+  const int st = moe_validate_config(cfg);
+  if (st != MOE_OK) return st;
+  const int32_t s = cfg->top_k < cfg->num_ranks ? cfg->top_k : cfg->num_ranks;
+  *rows = static_cast<int64_t>(cfg->num_tokens) * s;
+  return MOE_OK;
+}
+
+MOE_API int moe_combine_recv_two_level(moe_ctx* ctx, const float* topk_w, void* partial, int64_t partial_rows,
+                                       void* out, void* stream) {
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->phase != kCombineSent) return MOE_ESTATE;
+  const moe_config& c = ctx->cfg;
+  if (c.num_tokens > 0) {
+    int64_t need = 0;
+    moe_partial_rows(&c, &need);
+    if (partial_rows < need) return MOE_EINVAL;
+    if (!topk_w || !out || !partial || !aligned(topk_w, 4) || !aligned(out, 16) || !aligned(partial, 16))
+      return MOE_EINVAL;
+    moe::TwoLevelParams tp = {};
+    tp.y = static_cast<const uint8_t*>(ctx->expert_y);
+    tp.w = topk_w;
+    tp.slot_row = ctx->slot_row;
+    tp.rank_offsets = ctx->rank_offsets;
+    tp.partial = static_cast<uint8_t*>(partial);
+    tp.out = static_cast<uint8_t*>(out);
+    tp.plan_row = ctx->plan_row;
+    tp.plan_w = ctx->plan_w;
+    tp.plan_mask = ctx->plan_mask;
+    tp.T = c.num_tokens;
+    tp.K = c.top_k;
+    tp.H = c.hidden;
+    tp.N = c.num_ranks;
+    if (moe::launch_combine_two_level(tp, ctx->pdl != 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return MOE_ECUDA;
   }
   ctx->expert_y = nullptr;
   ctx->phase = kIdle;

@@ -141,6 +141,33 @@ size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K);
 BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem);
 cudaError_t launch_combine(const CombineParams& p, const CombineLaunch& l, cudaStream_t stream);
 
+// Two-stage dispatch: per-pair send rows and per-send-row grouped rows.
+struct StagedLayoutParams {
+  const int32_t* topk_idx;        // [T*K]
+  const int32_t* slot_row;        // [T*K]
+  const int32_t* expert_offsets;  // [E+1]
+  const int32_t* src_offsets;     // [E*N]
+  int32_t* send_pos;              // [T*K] send row of pair t*K+k (-1 after a routing error)
+  int32_t* send_dest;             // [T*K] grouped row of send row j (-1 after a routing error)
+  int32_t T, K, E, N;
+};
+cudaError_t launch_staged_layout(const StagedLayoutParams& p, bool pdl, cudaStream_t stream);
+
+// Two-level combine (partial sums on the sending side, then on the receiver).
+struct TwoLevelParams {
+  const uint8_t* y;             // [rows, H] bf16
+  const float* w;               // [T, K]
+  const int32_t* slot_row;      // [T*K]
+  const int32_t* rank_offsets;  // [N+1]
+  uint8_t* partial;             // [T*min(K,N), H] bf16
+  uint8_t* out;                 // [T, H] bf16
+  int32_t* plan_row;            // [T*K] the token's grouped rows, sorted by (rank, k)
+  float* plan_w;                // [T*K] their weights
+  int32_t* plan_mask;           // [T] bit i: sorted slot i ends a rank's group (0: routing error)
+  int32_t T, K, H, N;
+};
+cudaError_t launch_combine_two_level(const TwoLevelParams& p, bool pdl, cudaStream_t stream);
+
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` (and, if
 // asked, allows non-portable cluster sizes) on the current device.  Each
 // (kernel, device) pair pays the runtime call once; later launches only look

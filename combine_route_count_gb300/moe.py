@@ -30,13 +30,15 @@ COMBINE_BULK, COMBINE_VECTOR = 0, 1
 MOE_OPT_PACK_PREFETCH = 12
 MOE_OPT_CACHE_HINTS = 13
 MOE_OPT_PACK_STORE_DEPTH = 14
+MOE_OPT_MAX_SMS = 15
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.
 EXPORTS = ("moe_validate_config", "moe_workspace_bytes", "moe_recv_bound_rows", "moe_ctx_create",
            "moe_ctx_destroy", "moe_ctx_set_option", "moe_ctx_get_option", "moe_dispatch_send", "moe_dispatch_recv",
            "moe_combine_send", "moe_combine_recv", "moe_get_error", "moe_strerror",
-           "moe_dispatch_send_noalloc", "moe_dispatch_send_fp8")
+           "moe_dispatch_send_noalloc", "moe_dispatch_send_fp8", "moe_combine_recv_two_level", "moe_partial_rows",
+           "moe_dispatch_send_staged")
 
 
 class moe_config(ctypes.Structure):
@@ -81,9 +83,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_ctx_get_option": ([P, I, ctypes.POINTER(ctypes.c_int64)], I),
         "moe_dispatch_send": ([P, P, P, P, I64, P], I),
         "moe_dispatch_send_fp8": ([P, P, P, P, P, I64, P], I),
+        "moe_dispatch_send_staged": ([P, P, P, P, I64, P, I64, P], I),
         "moe_dispatch_recv": ([P, ctypes.POINTER(moe_dispatch_layout), P], I),
         "moe_combine_send": ([P, P, I64, P], I),
         "moe_combine_recv": ([P, P, P, P], I),
+        "moe_combine_recv_two_level": ([P, P, P, I64, P, P], I),
+        "moe_partial_rows": ([C, ctypes.POINTER(ctypes.c_int64)], I),
         "moe_get_error": ([P, P], I),
         "moe_strerror": ([I], ctypes.c_char_p),
     }
@@ -174,6 +179,13 @@ def moe_dispatch_send_fp8(ctx: int, x: Any, topk_idx: Any, expert_xq: Any, exper
                                                 expert_rows, _stream(stream)), "moe_dispatch_send_fp8")
 
 
+def moe_dispatch_send_staged(ctx: int, x: Any, topk_idx: Any, send_buf: Any, send_rows: int, expert_x: Any,
+                             expert_x_rows: int, stream: Any = None) -> None:
+    _check(load_library().moe_dispatch_send_staged(ctx, _ptr(x), _ptr(topk_idx), _ptr(send_buf), send_rows,
+                                                   _ptr(expert_x), expert_x_rows, _stream(stream)),
+           "moe_dispatch_send_staged")
+
+
 def moe_dispatch_recv(ctx: int, stream: Any = None) -> moe_dispatch_layout:
     lay = moe_dispatch_layout()
     _check(load_library().moe_dispatch_recv(ctx, ctypes.byref(lay), _stream(stream)), "moe_dispatch_recv")
@@ -186,6 +198,18 @@ def moe_combine_send(ctx: int, expert_y: Any, expert_y_rows: int, stream: Any = 
 
 def moe_combine_recv(ctx: int, topk_w: Any, out: Any, stream: Any = None) -> None:
     _check(load_library().moe_combine_recv(ctx, _ptr(topk_w), _ptr(out), _stream(stream)), "moe_combine_recv")
+
+
+def moe_combine_recv_two_level(ctx: int, topk_w: Any, partial: Any, partial_rows: int, out: Any,
+                               stream: Any = None) -> None:
+    _check(load_library().moe_combine_recv_two_level(ctx, _ptr(topk_w), _ptr(partial), partial_rows, _ptr(out),
+                                                     _stream(stream)), "moe_combine_recv_two_level")
+
+
+def moe_partial_rows(cfg: moe_config) -> int:
+    v = ctypes.c_int64(0)
+    _check(load_library().moe_partial_rows(ctypes.byref(cfg), ctypes.byref(v)), "moe_partial_rows")
+    return int(v.value)
 
 
 def moe_get_error(ctx: int, stream: Any = None) -> int:
@@ -283,7 +307,8 @@ class MoELayer:
                  "combine_variant": MOE_OPT_COMBINE_VARIANT, "combine_stages": MOE_OPT_COMBINE_STAGES,
                  "combine_piece_bytes": MOE_OPT_COMBINE_PIECE_BYTES,
                  "combine_ctas_per_sm": MOE_OPT_COMBINE_CTAS_PER_SM, "pack_prefetch": MOE_OPT_PACK_PREFETCH,
-                 "cache_hints": MOE_OPT_CACHE_HINTS, "pack_store_depth": MOE_OPT_PACK_STORE_DEPTH}
+                 "cache_hints": MOE_OPT_CACHE_HINTS, "pack_store_depth": MOE_OPT_PACK_STORE_DEPTH,
+                 "max_sms": MOE_OPT_MAX_SMS}
         for k, v in options.items():
             moe_ctx_set_option(self.ctx, names[k], int(v))
 
@@ -316,6 +341,11 @@ class MoELayer:
         """fp8 payload: expert_xq uint8 [>= T*K, H], expert_scales float32 [>= T*K, H/128]."""
         moe_dispatch_send_fp8(self.ctx, x, topk_idx, expert_xq, expert_scales, expert_xq.shape[0], stream)
 
+    def dispatch_send_staged(self, x, topk_idx, send_buf, expert_x, stream: Any = None) -> None:
+        """Two-stage dispatch: send_buf bf16 [>= T*K, H] is caller scratch."""
+        moe_dispatch_send_staged(self.ctx, x, topk_idx, send_buf, send_buf.shape[0], expert_x, expert_x.shape[0],
+                                 stream)
+
     def dispatch_recv(self, stream: Any = None) -> "DispatchLayout":
         """The dispatch layout; its arrays are torch views into the workspace,
         made on first access (the call itself only crosses the C ABI)."""
@@ -326,6 +356,13 @@ class MoELayer:
 
     def combine_recv(self, topk_w, out, stream: Any = None) -> None:
         moe_combine_recv(self.ctx, topk_w, out, stream)
+
+    def combine_recv_two_level(self, topk_w, partial, out, stream: Any = None) -> None:
+        """Two-level combine: partial bf16 [>= T*min(K,N), H] is caller scratch."""
+        moe_combine_recv_two_level(self.ctx, topk_w, partial, partial.shape[0], out, stream)
+
+    def partial_rows(self) -> int:
+        return moe_partial_rows(self.cfg)
 
     def get_error(self, stream: Any = None) -> int:
         return moe_get_error(self.ctx, stream)

@@ -90,7 +90,8 @@ typedef struct moe_dispatch_layout {
 int moe_validate_config(const moe_config* cfg);
 
 /* Device workspace (bytes, a multiple of 256) that one context needs: counts,
- * offsets, slot_row, row_src and the error word.  Allocate it 256-byte
+ * offsets, slot_row, row_src, the error word, the send tables of
+ * moe_dispatch_send_staged and the plan of moe_combine_recv_two_level.  Allocate it 256-byte
  * aligned; its contents need no initialisation. */
 int moe_workspace_bytes(const moe_config* cfg, size_t* bytes);
 
@@ -145,6 +146,26 @@ int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void
 int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_xq,
                           float* expert_scales, int64_t expert_rows, void* stream);
 
+/* Dispatch, send half, two-stage form ("Enabling trillion-parameter models on
+ * AWS EFA", dispatch and combine timing: the sender copies tokens into
+ * contiguous per-peer send buffers at offsets from the cumulative sum of its
+ * per-expert counts; the receiver then shuffles them from its receive buffer
+ * into the grouped-GEMM input).  Same routing and same results as
+ * moe_dispatch_send, which writes every row straight to its grouped position
+ * (send and receive memory are one on a single GPU); this form keeps the
+ * pages' extra copy so that its cost can be measured.  Enqueues routing, a
+ * send-layout kernel and two pack kernels:
+ *   stage 1: source rank s's (token, slot) pairs, in (expert, token) order,
+ *            go to send rows [s*T/N*K, (s+1)*T/N*K) of send_buf (x rows);
+ *   stage 2: every send row is copied to its row of expert_x.
+ *   send_buf   device bf16 [send_rows, H], send_rows >= T*K, 16-byte aligned,
+ *              caller-owned scratch (only rows [0, T*K) are written)
+ *   x, topk_idx, expert_x, expert_x_rows  as for moe_dispatch_send
+ * Errors as for moe_dispatch_send; after a routing error nothing is written to
+ * send_buf or expert_x.  Valid in the idle phase; moe_dispatch_recv follows. */
+int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* send_buf, int64_t send_rows,
+                             void* expert_x, int64_t expert_x_rows, void* stream);
+
 /* Dispatch, receive half.  On one GPU the send half already placed every row
  * in the grouped layout (the shared-buffer case of "Efficient and portable
  * mixture-of-experts communication", Further improvements), so this enqueues
@@ -170,6 +191,34 @@ int moe_combine_send(moe_ctx* ctx, const void* expert_y, int64_t expert_y_rows, 
  *   out     device bf16 [T, H]
  * Valid after moe_combine_send; returns the context to the idle phase. */
 int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void* stream);
+
+/* Combine, receive half, two-level form: partial sums on the sending side
+ * ("Enabling trillion-parameter models on AWS EFA", evaluation, prefill:
+ * DeepEP adds a token's expert outputs on the sender to move less data, which
+ * can cost precision; moe_combine_recv adds only at the receiver).  An
+ * alternative to moe_combine_recv, for measuring that trade.  Enqueues a
+ * plan kernel (each token's slots sorted by rank) and two reduction kernels:
+ *   level 1: for each token t and each rank r holding some of its experts,
+ *     partial = bf16_rne( fma chain over those experts in top-k order of
+ *                         topk_w[t, k] * expert_y[slot_row[t, k], h], from +0.0f )
+ *     written to partial row t*min(K,N) + d, d = the position of r among the
+ *     token's ranks in ascending order;
+ *   level 2: out[t, h] = bf16_rne( float32 sum of the token's partials in
+ *                                  ascending rank order, from +0.0f ).
+ *   topk_w        device float32 [T, K], 4-byte aligned
+ *   partial       device bf16 [partial_rows, H], 16-byte aligned, caller-owned
+ *                 scratch; partial_rows >= T*min(K,N) (moe_partial_rows);
+ *                 rows a token does not use are left untouched
+ *   out           device bf16 [T, H]
+ * A token whose routing failed (MOE_EROUTE) gets nothing written.  Returns
+ * MOE_EINVAL for a short or misaligned buffer.  Valid after moe_combine_send;
+ * returns the context to the idle phase. */
+int moe_combine_recv_two_level(moe_ctx* ctx, const float* topk_w, void* partial, int64_t partial_rows, void* out,
+                               void* stream);
+
+/* Rows of the partial buffer moe_combine_recv_two_level needs: T*min(K,N).
+ * Returns MOE_EINVAL for an invalid configuration. */
+int moe_partial_rows(const moe_config* cfg, int64_t* rows);
 
 /* Launch options of one context (tuning knobs; the defaults are the tuned
  * configuration).  Returns MOE_EINVAL for an unknown option or value.
@@ -227,8 +276,19 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               (default 7: all streamed data) */
 #define MOE_OPT_CACHE_HINTS 13
 /*   MOE_OPT_PACK_STORE_DEPTH    bulk pack: store groups left in flight before a
- *                               stage is refilled, 1..8 (0 = default, 1) */
+ *                               stage is refilled, 1..8 (0 = default, 2) */
 #define MOE_OPT_PACK_STORE_DEPTH 14
+/*   MOE_OPT_MAX_SMS             sizes the persistent pack and combine grids
+ *                               (bulk and fp8 pack, bulk combine) for this
+ *                               many SMs instead of all of them (CTAs = SMs
+ *                               x CTAs per SM), so that they hold only that
+ *                               share of the GPU's shared memory and warps
+ *                               and work the caller runs on another stream
+ *                               can be resident at the same time; 0 = all
+ *                               (default), else 1..SM count.  The flat
+ *                               vector kernels and the two-level combine are
+ *                               not bounded by it. */
+#define MOE_OPT_MAX_SMS 15
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
 /* ---- Dispatch without any device allocation ------------------------------
