@@ -163,6 +163,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of every rank's value (all ranks get it); the value itself
+    with one rank.  NCCL wants a device tensor, gloo a host one."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_layer(step_us_max: float, world_size: int) -> float:
+    """Whole-job µs per layer: every replica runs one layer per step, so the
+    job finishes world_size layers in the slowest rank's step time."""
+    return step_us_max / max(world_size, 1)
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -349,13 +367,8 @@ def run_gpu(args):
     if status != moe.MOE_OK:
         raise RuntimeError(f"device reported status {status} in the timed region")
     total_ms = t_start.elapsed_time(t_end)
-    ms_step = total_ms / args.steps
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
-    us_layer = ms_step * 1e3
+    ms_step = max_over_ranks(total_ms / args.steps, dev)  # slowest replica
+    us_layer = job_us_per_layer(ms_step * 1e3, ws)
 
     # Attribution pass (not the headline): the same steps with an event
     # before dispatch_send, between dispatch_send and combine_recv, and after.
@@ -441,7 +454,7 @@ def run_gpu(args):
                                    3: f"route_cluster ({layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS)} CTAs)"}[
                            layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)]},
             "achieved_gbs": round(ab["total"] / us_layer / 1e3, 1),
-            "hbm_frac": round(ab["total"] / us_layer / 1e3 / peak, 4),
+            "hbm_frac": round(ab["total"] / us_layer / 1e3 / (peak * ws), 4),  # per GPU
             "algorithmic_bytes_per_layer": ab["total"],
             "kernels": kernels,
             "roofline": roofline,

@@ -563,10 +563,12 @@ int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, const int32_t* table,
   }
   pl.pdl = pdl;
   pl.hints = ctx->cache_hints;
-  // Two store groups in flight by default (measured on GB300 with the
-  // destination rows loaded one unit ahead: DeepSeek-, worst-case- and
-  // Mixtral-sized layers and the two-stage dispatch gain over one).
-  pl.depth = ctx->pack_depth > 0 ? ctx->pack_depth : 2;
+  // Store groups in flight (measured on GB300 with the destination rows
+  // loaded one unit ahead): two for DeepSeek-, worst-case- and Mixtral-sized
+  // layers and the two-stage dispatch; one when the pack writes more than
+  // 1 GiB (Kimi-sized layers: 3 % faster than with two).
+  const int64_t dest_bytes = static_cast<int64_t>(T) * K * pp.row_bytes;
+  pl.depth = ctx->pack_depth > 0 ? ctx->pack_depth : (dest_bytes > (int64_t{1} << 30) ? 1 : 2);
   if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
   return MOE_OK;
 }

@@ -276,7 +276,8 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               (default 7: all streamed data) */
 #define MOE_OPT_CACHE_HINTS 13
 /*   MOE_OPT_PACK_STORE_DEPTH    bulk pack: store groups left in flight before a
- *                               stage is refilled, 1..8 (0 = default, 2) */
+ *                               stage is refilled, 1..8 (0 = automatic:
+ *                               2, or 1 when a pack writes more than 1 GiB) */
 #define MOE_OPT_PACK_STORE_DEPTH 14
 /*   MOE_OPT_MAX_SMS             sizes the persistent pack and combine grids
  *                               (bulk and fp8 pack, bulk combine) for this
