@@ -414,8 +414,8 @@ int pack_piece_bytes(const moe_ctx* c, int64_t row_bytes) {
   return static_cast<int>(pb);
 }
 
-int pack_grid(const moe_ctx* c, const moe::PackParams& p, int stages) {
-  const bool bulk = c->pack_variant == moe::kPackBulk;
+int pack_grid(const moe_ctx* c, const moe::PackParams& p, int variant, int stages) {
+  const bool bulk = variant == moe::kPackBulk;
   const int64_t units = static_cast<int64_t>(p.T) * p.pieces;
   int per_sm = c->pack_ctas_per_sm > 0 ? c->pack_ctas_per_sm : (bulk ? pack_ctas_auto(p.K) : 0);
   if (bulk) {
@@ -511,9 +511,10 @@ namespace {
 // bulk pack reads its first source rows before waiting on the previous
 // kernel, so `pdl` must be false when src is that kernel's output.
 // `prefetch` allows the context's L2 prefetch of source rows (which pays
-// while the pack overlaps routing).
+// while the pack overlaps routing); `variant` < 0 takes the context's pack
+// variant.
 int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, const int32_t* table, int32_t T, int32_t K,
-                 bool pdl, bool prefetch, cudaStream_t s) {
+                 bool pdl, bool prefetch, int variant, cudaStream_t s) {
   moe::PackParams pp = {};
   pp.x = static_cast<const uint8_t*>(src);
   pp.expert_x = static_cast<uint8_t*>(dst);
@@ -525,7 +526,7 @@ int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, const int32_t* table,
   pp.piece_bytes = pack_piece_bytes(ctx, pp.row_bytes);
   pp.pieces = static_cast<int32_t>((pp.row_bytes + pp.piece_bytes - 1) / pp.piece_bytes);
   moe::PackLaunch pl = {};
-  pl.variant = ctx->pack_variant;
+  pl.variant = variant >= 0 ? variant : ctx->pack_variant;
   pl.stages = ctx->pack_stages;
   if (pl.stages <= 0) {
     // About 100 KiB of stages per CTA (two CTAs per SM), 2..16 stages.
@@ -541,7 +542,7 @@ int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, const int32_t* table,
     if (moe::pack_bulk_smem_bytes(pl.stages, pp.piece_bytes) > static_cast<size_t>(ctx->max_smem_optin))
       return MOE_EINVAL;
   }
-  pl.grid = pack_grid(ctx, pp, pl.stages);
+  pl.grid = pack_grid(ctx, pp, pl.variant, pl.stages);
   pl.prefetch = prefetch ? ctx->pack_prefetch : 0;
   pl.prefetch_units = -1;
   if (pl.prefetch == 2) {
@@ -591,7 +592,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
   if (rrc != MOE_OK) return rrc;
 
   if (c.num_tokens > 0) {
-    const int prc = enqueue_pack(ctx, x, expert_x, ctx->slot_row, c.num_tokens, c.top_k, ctx->pdl != 0, true, s);
+    const int prc = enqueue_pack(ctx, x, expert_x, ctx->slot_row, c.num_tokens, c.top_k, ctx->pdl != 0, true, -1, s);
     if (prc != MOE_OK) return prc;
   }
   ctx->phase = kDispatched;
@@ -627,12 +628,15 @@ MOE_API int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t*
     sp.N = c.num_ranks;
     if (moe::launch_staged_layout(sp, ctx->pdl != 0, s) != cudaSuccess) return MOE_ECUDA;
     // Stage 1, every source rank: x rows into its per-peer send rows.
-    int prc = enqueue_pack(ctx, x, send_buf, ctx->send_pos, c.num_tokens, c.top_k, ctx->pdl != 0, true, s);
+    int prc = enqueue_pack(ctx, x, send_buf, ctx->send_pos, c.num_tokens, c.top_k, ctx->pdl != 0, true, -1, s);
     if (prc != MOE_OK) return prc;
     // Stage 2, every receiver: send rows into the grouped rows.  Its source is
     // the previous kernel's output, so it is not launched early, and there is
-    // nothing for an L2 prefetch to overlap.
-    prc = enqueue_pack(ctx, send_buf, expert_x, ctx->send_dest, static_cast<int32_t>(pairs), 1, false, false, s);
+    // nothing for an L2 prefetch to overlap.  One destination per row: the
+    // 16-byte vector copy is used (measured faster on GB300 than the bulk
+    // pipeline, which moves one row piece per stage cycle when K = 1).
+    prc = enqueue_pack(ctx, send_buf, expert_x, ctx->send_dest, static_cast<int32_t>(pairs), 1, false, false,
+                       moe::kPackVector, s);
     if (prc != MOE_OK) return prc;
   }
   ctx->phase = kDispatched;
@@ -666,10 +670,16 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
     fp.T = c.num_tokens;
     fp.K = c.top_k;
     fp.H = c.hidden;
-    // MOE_OPT_PACK_STAGES / _CTAS_PER_SM apply here too; automatic: about
-    // 72 KiB of row stages per CTA, three CTAs (12 consumer warps) per SM.
+    // MOE_OPT_PACK_STAGES / _CTAS_PER_SM apply here too.  Automatic, K >= 4:
+    // about 72 KiB of row stages per CTA, three CTAs (12 consumer warps) per
+    // SM.  K < 4: each token row carries little write traffic for the
+    // quantisation work it needs, so more CTAs work on tokens side by side:
+    // three stages, up to eight CTAs per SM (measured on GB300, Mixtral-sized
+    // layers: 8 % faster per layer than three CTAs).
+    const bool few_dest = c.top_k < 4;
     int stages = ctx->pack_stages > 0 ? ctx->pack_stages
-                                      : static_cast<int>((72 * 1024) / (static_cast<int64_t>(c.hidden) * 2));
+                 : few_dest         ? 3
+                                    : static_cast<int>((72 * 1024) / (static_cast<int64_t>(c.hidden) * 2));
     const int maxst = moe::pack_fp8_max_stages();
     if (stages > maxst) stages = maxst;
     if (stages < 2) stages = 2;
@@ -677,7 +687,7 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
       --stages;
     const size_t smem = moe::pack_fp8_smem_bytes(stages, c.hidden);
     int per_sm = static_cast<int>((228 * 1024) / (smem + 1024));
-    const int want = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : 3;
+    const int want = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : (few_dest ? 8 : 3);
     if (per_sm > want) per_sm = want;
     if (per_sm < 1) per_sm = 1;
     int64_t grid = static_cast<int64_t>(grid_sms(ctx)) * per_sm;

@@ -224,13 +224,16 @@ int moe_partial_rows(const moe_config* cfg, int64_t* rows);
  * configuration).  Returns MOE_EINVAL for an unknown option or value.
  *   MOE_OPT_PACK_VARIANT      0 = bulk copies through shared memory (TMA
  *                             engine, default), 1 = 16-byte vector loads/stores
+ *                             (the receive shuffle of moe_dispatch_send_staged
+ *                             always uses the vector copy)
  *   MOE_OPT_PACK_STAGES       shared-memory stages per bulk CTA, 2..16, 0 =
- *                             automatic (about 200 KiB of stages per SM, default)
+ *                             automatic (about 200 KiB of stages per SM, default;
+ *                             fp8 pack: about 72 KiB per CTA for K >= 4, else 3)
  *   MOE_OPT_PACK_PIECE_BYTES  bytes of a row moved per work unit, a multiple of
  *                             16, 0 = automatic (whole row up to 8 KiB, else
  *                             equal pieces of at most 8 KiB)
- *   MOE_OPT_PACK_CTAS_PER_SM  0 = automatic (bulk variant: 2 for K >= 4, else 3),
- *                             else 1..32
+ *   MOE_OPT_PACK_CTAS_PER_SM  0 = automatic (bulk variant: 2 for K >= 4, else 3;
+ *                             fp8 pack: 3 for K >= 4, else up to 8), else 1..32
  *   MOE_OPT_PDL               1 = launch pack/combine with programmatic
  *                             dependent launch (default), 0 = plain launches
  *   MOE_OPT_ROUTE_VARIANT     routing kernels: 0 = automatic (route_cluster
