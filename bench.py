@@ -370,6 +370,18 @@ def run_gpu(args):
     ms_step = max_over_ranks(total_ms / args.steps, dev)  # slowest replica
     us_layer = job_us_per_layer(ms_step * 1e3, ws)
 
+    # Warm-L2 figure (not the headline): the same steps on one buffer set, so
+    # whatever of the previous step's data is still in L2 is reused.
+    n_warm = min(args.steps, 500)
+    torch.cuda.synchronize(dev)
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for _ in range(n_warm):
+        step(sets[0])
+    w1.record(stream)
+    torch.cuda.synchronize(dev)
+    l2_warm_us = w0.elapsed_time(w1) / n_warm * 1e3
+
     # Attribution pass (not the headline).  Each dispatch_send is timed
     # between its own two events.  An event between dispatch_send and
     # combine_recv would break their programmatic dependent launch and charge
@@ -475,6 +487,7 @@ def run_gpu(args):
                        "routing": {1: "route_count (1 block)", 2: "route_local+route_finalize",
                                    3: f"route_cluster ({layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS)} CTAs)"}[
                            layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)]},
+            "l2_warm_us": round(l2_warm_us, 2),
             "achieved_gbs": round(ab["total"] / us_layer / 1e3, 1),
             "hbm_frac": round(ab["total"] / us_layer / 1e3 / (peak * ws), 4),  # per GPU
             "algorithmic_bytes_per_layer": ab["total"],
