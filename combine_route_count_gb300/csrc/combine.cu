@@ -198,6 +198,9 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
           break;
         }
       }
+      // Failure-injection hook (tests only): nothing is posted for this unit,
+      // so its consumers' bounded wait runs out and reports MOE_ETIMEDOUT.
+      if (u == sh.drop_unit) continue;
       const bool bad = __any_sync(0xffffffffu, lane < K && row < 0);
       const uint32_t bytes = piece_len(j);
       if (lane == 0) {
@@ -303,6 +306,7 @@ size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K) {
 BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem) {
   BulkCombineShape sh;
   sh.hints = 0;
+  sh.drop_unit = -1;
   const int64_t row_bytes = static_cast<int64_t>(H) * 2;
   if (piece_bytes <= 0) {
     // Pieces of at most 2 KiB (128 consumer threads), equal up to 16 bytes.
@@ -319,7 +323,7 @@ BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, i
   }
   if (stages < 2) stages = 2;
   if (stages > kMaxBulkStages) stages = kMaxBulkStages;
-  while (stages > 2 && combine_bulk_smem_bytes(BulkCombineShape{stages, sh.piece_bytes, sh.pieces, 0}, K) >
+  while (stages > 2 && combine_bulk_smem_bytes(BulkCombineShape{stages, sh.piece_bytes, sh.pieces, 0, -1}, K) >
                            static_cast<size_t>(max_smem))
     --stages;
   sh.stages = stages;

@@ -125,6 +125,7 @@ struct moe_ctx {
   int device;
   int num_sms;
   int max_sms;  // MOE_OPT_MAX_SMS: 0 = every SM
+  int64_t test_drop_unit;  // MOE_OPT_TEST_DROP_COMBINE_UNIT (-1: off)
   int max_smem_optin;
   int l2_bytes;
   int phase;
@@ -247,6 +248,7 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->pdl = 1;
   c->route_variant = 0;
   c->combine_variant = -1;  // automatic
+  c->test_drop_unit = -1;
   // Largest cluster of route_cluster CTAs this device can schedule for this
   // configuration (16, else 8, 4, 2, 1), or none.
   for (int maxc = moe::kMaxClusterCtas; maxc >= 1; maxc /= 2) {
@@ -352,6 +354,10 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       if (value < 0 || value > ctx->num_sms) return MOE_EINVAL;
       ctx->max_sms = static_cast<int>(value);
       return MOE_OK;
+    case MOE_OPT_TEST_DROP_COMBINE_UNIT:
+      if (value < -1) return MOE_EINVAL;
+      ctx->test_drop_unit = value;
+      return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       if (value < 0 || value > 3) return MOE_EINVAL;
       if (value == 3 && ctx->cluster_ctas == 0) return MOE_EINVAL;
@@ -409,6 +415,9 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
       return MOE_OK;
     case MOE_OPT_MAX_SMS:
       *value = ctx->max_sms;
+      return MOE_OK;
+    case MOE_OPT_TEST_DROP_COMBINE_UNIT:
+      *value = ctx->test_drop_unit;
       return MOE_OK;
     default:
       return MOE_EINVAL;
@@ -773,6 +782,7 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
       cl.shape = moe::combine_bulk_shape(c.hidden, c.top_k, ctx->combine_stages, ctx->combine_piece_bytes,
                                          ctx->max_smem_optin);
       cl.shape.hints = ctx->cache_hints;
+      cl.shape.drop_unit = ctx->test_drop_unit;
       const size_t smem = moe::combine_bulk_smem_bytes(cl.shape, c.top_k);
       if (smem > static_cast<size_t>(ctx->max_smem_optin)) return MOE_EINVAL;
       const int fit = static_cast<int>((228 * 1024) / (smem + 1024));

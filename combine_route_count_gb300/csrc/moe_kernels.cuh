@@ -126,10 +126,11 @@ struct CombineParams {
 };
 enum CombineVariant { kCombineBulk = 0, kCombineVector = 1 };
 struct BulkCombineShape {
-  int stages;       // shared-memory stages per CTA
-  int piece_bytes;  // bytes of a row per unit (multiple of 16)
-  int pieces;       // units per token
-  int hints;        // CacheHints
+  int stages;          // shared-memory stages per CTA
+  int piece_bytes;     // bytes of a row per unit (multiple of 16)
+  int pieces;          // units per token
+  int hints;           // CacheHints
+  int64_t drop_unit;   // failure-injection hook: unit the producer never posts (-1: none)
 };
 struct CombineLaunch {
   int variant;             // CombineVariant

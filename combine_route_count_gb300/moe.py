@@ -31,6 +31,7 @@ MOE_OPT_PACK_PREFETCH = 12
 MOE_OPT_CACHE_HINTS = 13
 MOE_OPT_PACK_STORE_DEPTH = 14
 MOE_OPT_MAX_SMS = 15
+MOE_OPT_TEST_DROP_COMBINE_UNIT = 16
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.

@@ -293,6 +293,17 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               vector kernels and the two-level combine are
  *                               not bounded by it. */
 #define MOE_OPT_MAX_SMS 15
+/*   MOE_OPT_TEST_DROP_COMBINE_UNIT  failure-injection hook for tests, -1 = off
+ *                               (default).  With a unit index u >= 0 (token
+ *                               u / pieces, piece u % pieces), the bulk
+ *                               combine's producer never posts unit u, so the
+ *                               consumers' bounded wait (2 s) runs out: the
+ *                               combine writes nothing for the rest of that
+ *                               CTA's units, reports MOE_ETIMEDOUT in the error
+ *                               word and returns; the context stays usable
+ *                               (the next dispatch resets the error word).
+ *                               Only the bulk combine variant honours it. */
+#define MOE_OPT_TEST_DROP_COMBINE_UNIT 16
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
 /* ---- Dispatch without any device allocation ------------------------------

@@ -69,7 +69,7 @@ def check(res, oracle_mod, w, li):
         assert np.array_equal(res["out"], oracle_mod.combine(li.y, li.topk_w, d.slot_row))
 
 
-@pytest.mark.parametrize("name", ["tiny", "mixtral", "deepseek", "worst"])
+@pytest.mark.parametrize("name", [w.name for w in gen.WORKLOADS])
 def test_staged_named_workloads(moe, oracle_mod, name):
     w = gen.BY_NAME[name]
     li = gen.make_inputs(w)

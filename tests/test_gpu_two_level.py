@@ -70,7 +70,7 @@ def check(res, oracle_mod, w, li):
     return nr
 
 
-@pytest.mark.parametrize("name", ["tiny", "mixtral", "deepseek", "worst"])
+@pytest.mark.parametrize("name", [w.name for w in gen.WORKLOADS])
 def test_two_level_named_workloads(moe, oracle_mod, name):
     w = gen.BY_NAME[name]
     li = gen.make_inputs(w)
