@@ -170,7 +170,8 @@ int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t* topk_id
  * in the grouped layout (the shared-buffer case of "Efficient and portable
  * mixture-of-experts communication", Further improvements), so this enqueues
  * nothing: it fills `layout` with device pointers to the counts, offsets and
- * routing tables.  Valid after moe_dispatch_send. */
+ * routing tables.  Valid after moe_dispatch_send, moe_dispatch_send_fp8 or
+ * moe_dispatch_send_staged. */
 int moe_dispatch_recv(moe_ctx* ctx, moe_dispatch_layout* layout, void* stream);
 
 /* Combine, send half: registers the expert outputs, one row per dispatched
