@@ -136,8 +136,11 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
 // DROP = true only for the failure-injection hook: a separate instance, since
 // even this one warp-uniform compare in the producer's per-unit path was
 // measured to slow the normal kernel down (DeepSeek-sized layer 168.8 ->
-// 170.9 us).
-template <int KMAX, bool DROP>
+// 170.9 us).  STRIDED picks the tokens of a CTA: false = one contiguous range
+// of units; true = tokens b, b+G, b+2G, ... (G CTAs), all pieces of each, so
+// that the CTAs work on a window of consecutive tokens at any moment and the
+// rows they gather sit close together inside each expert's region.
+template <int KMAX, bool DROP, bool STRIDED>
 __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(CombineParams p, BulkCombineShape sh) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -151,11 +154,31 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int consumer_warps = (blockDim.x >> 5) - 1;
 
-  // Contiguous unit range of this CTA.
-  const int64_t units = static_cast<int64_t>(p.T) * P;
-  const int64_t q = units / gridDim.x, rem = units % gridDim.x;
-  const int64_t u0 = blockIdx.x * q + (blockIdx.x < rem ? blockIdx.x : rem);
-  const int64_t n = q + (blockIdx.x < rem ? 1 : 0);
+  // Units of this CTA: a contiguous range starting at u0, or (STRIDED) all
+  // pieces of tokens blockIdx.x + m * gridDim.x.
+  const int64_t G = gridDim.x;
+  int64_t u0, n;
+  if constexpr (STRIDED) {
+    u0 = static_cast<int64_t>(blockIdx.x) * P;
+    n = (p.T > blockIdx.x ? (p.T - blockIdx.x + G - 1) / G : 0) * P;
+  } else {
+    const int64_t units = static_cast<int64_t>(p.T) * P;
+    const int64_t q = units / G, rem = units % G;
+    u0 = blockIdx.x * q + (blockIdx.x < rem ? blockIdx.x : rem);
+    n = q + (blockIdx.x < rem ? 1 : 0);
+  }
+  // (token, piece) of the CTA's i-th unit.
+  auto unit_at = [&](int64_t i, int64_t& t, int& j) {
+    if constexpr (STRIDED) {
+      const int64_t m = i / P;
+      j = static_cast<int>(i - m * P);
+      t = blockIdx.x + m * G;
+    } else {
+      const int64_t u = u0 + i;
+      t = u / P;
+      j = static_cast<int>(u - t * P);
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -179,21 +202,26 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
     int64_t t_cur = -1;
     int row = -1, next_row = -1;
     if (n > 0 && lane < K) {
-      const int64_t t0 = u0 / P;
+      const int64_t t0 = STRIDED ? static_cast<int64_t>(blockIdx.x) : u0 / P;
       next_row = p.slot_row[t0 * K + lane];
     }
     bool ok = true;
     for (int64_t i = 0; i < n; ++i) {
       const int s = static_cast<int>(i % S);
-      const int64_t u = u0 + i;
-      const int64_t t = u / P;
-      const int j = static_cast<int>(u - t * P);
+      int64_t t;
+      int j;
+      unit_at(i, t, j);
       if (t != t_cur) {
         t_cur = t;
         row = next_row;
         // Prefetch the next token's rows while this one is in flight.
-        const int64_t tn = t + 1;
-        if (lane < K && tn * P < u0 + n) next_row = p.slot_row[tn * K + lane];
+        if constexpr (STRIDED) {
+          const int64_t tn = t + G;
+          if (lane < K && tn < p.T) next_row = p.slot_row[tn * K + lane];
+        } else {
+          const int64_t tn = t + 1;
+          if (lane < K && tn * P < u0 + n) next_row = p.slot_row[tn * K + lane];
+        }
       }
       if (i >= S) {
         const bool freed = wait_parity(&empty[s], static_cast<uint32_t>(((i / S) - 1) & 1));
@@ -204,7 +232,7 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
       }
       // Failure-injection hook (tests only): nothing is posted for this unit,
       // so its consumers' bounded wait runs out and reports MOE_ETIMEDOUT.
-      if (DROP && u == sh.drop_unit) continue;
+      if (DROP && t * P + j == sh.drop_unit) continue;
       const bool bad = __any_sync(0xffffffffu, lane < K && row < 0);
       const uint32_t bytes = piece_len(j);
       if (lane == 0) {
@@ -233,9 +261,9 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
     float wk[KMAX];
     for (int64_t i = 0; i < n; ++i) {
       const int s = static_cast<int>(i % S);
-      const int64_t u = u0 + i;
-      const int64_t t = u / P;
-      const int j = static_cast<int>(u - t * P);
+      int64_t t;
+      int j;
+      unit_at(i, t, j);
       if (t != t_cur) {
         t_cur = t;
 #pragma unroll
@@ -283,7 +311,10 @@ template <int KMAX>
 cudaError_t launch_bulk_k(const CombineParams& p, const CombineLaunch& l, cudaStream_t stream) {
   const BulkCombineShape& sh = l.shape;
   const size_t smem = combine_bulk_smem_bytes(sh, p.K);
-  auto* kern = sh.drop_unit >= 0 ? combine_bulk_kernel<KMAX, true> : combine_bulk_kernel<KMAX, false>;
+  auto* kern = sh.strided ? (sh.drop_unit >= 0 ? combine_bulk_kernel<KMAX, true, true>
+                                              : combine_bulk_kernel<KMAX, false, true>)
+                          : (sh.drop_unit >= 0 ? combine_bulk_kernel<KMAX, true, false>
+                                              : combine_bulk_kernel<KMAX, false, false>);
   cudaError_t err = set_kernel_limits(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   const int threads = 32 + (sh.piece_bytes / 16 + 31) / 32 * 32;
@@ -307,14 +338,16 @@ size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K) {
   return kBulkBarBytes + static_cast<size_t>(sh.stages) * K * sh.piece_bytes;
 }
 
-BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem) {
+BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem, int auto_piece_max) {
   BulkCombineShape sh;
   sh.hints = 0;
   sh.drop_unit = -1;
+  sh.strided = 0;
   const int64_t row_bytes = static_cast<int64_t>(H) * 2;
   if (piece_bytes <= 0) {
-    // Pieces of at most 2 KiB (128 consumer threads), equal up to 16 bytes.
-    const int64_t pieces = (row_bytes + 2048 - 1) / 2048;
+    // Pieces of at most auto_piece_max bytes (one consumer thread per 16
+    // bytes), equal up to 16 bytes.
+    const int64_t pieces = (row_bytes + auto_piece_max - 1) / auto_piece_max;
     piece_bytes = static_cast<int>((row_bytes / 16 + pieces - 1) / pieces * 16);
   }
   if (piece_bytes > kBulkMaxPiece) piece_bytes = kBulkMaxPiece;
@@ -327,7 +360,7 @@ BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, i
   }
   if (stages < 2) stages = 2;
   if (stages > kMaxBulkStages) stages = kMaxBulkStages;
-  while (stages > 2 && combine_bulk_smem_bytes(BulkCombineShape{stages, sh.piece_bytes, sh.pieces, 0, -1}, K) >
+  while (stages > 2 && combine_bulk_smem_bytes(BulkCombineShape{stages, sh.piece_bytes, sh.pieces, 0, -1, 0}, K) >
                            static_cast<size_t>(max_smem))
     --stages;
   sh.stages = stages;

@@ -131,6 +131,7 @@ struct BulkCombineShape {
   int pieces;          // units per token
   int hints;           // CacheHints
   int64_t drop_unit;   // failure-injection hook: unit the producer never posts (-1: none)
+  int strided;         // 1: a CTA takes tokens b, b+G, ...; 0: a contiguous unit range
 };
 struct CombineLaunch {
   int variant;             // CombineVariant
@@ -139,7 +140,9 @@ struct CombineLaunch {
   bool pdl;                // launch with programmatic stream serialization
 };
 size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K);
-BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem);
+// Stages and pieces of the bulk combine; piece_bytes <= 0 picks equal pieces
+// of at most auto_piece_max bytes (a multiple of 16, at most 4096).
+BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem, int auto_piece_max);
 cudaError_t launch_combine(const CombineParams& p, const CombineLaunch& l, cudaStream_t stream);
 
 // Two-stage dispatch: per-pair send rows and per-send-row grouped rows.

@@ -163,6 +163,9 @@ PACK_OPTIONS = [
     dict(pack_stages=14, pack_ctas_per_sm=2, combine_stages=5),
     dict(pack_store_depth=1),
     dict(pack_store_depth=5, pack_stages=6),
+    dict(combine_variant=0, combine_order=1),
+    dict(combine_variant=0, combine_order=1, combine_piece_bytes=2048 + 16, combine_stages=3, combine_ctas_per_sm=3),
+    dict(combine_variant=0, combine_order=0),
 ]
 
 
@@ -220,6 +223,16 @@ def test_empty_layer(moe):
     assert lay["expert_offsets"].cpu().tolist() == [0] * 9
     assert lay["src_offsets"].cpu().numpy().tolist() == [[0, 0]] * 8
     assert _intact(big, 0)
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=["x".join(map(str, s[:5])) for s in EDGE])
+def test_edge_shapes_strided_combine(moe, oracle_mod, shape):
+    T, H, K, E, N, router = shape
+    w = gen.custom("edge", T=T, H=H, K=K, E=E, N=N, router=router, seed_index=13)
+    li = gen.make_inputs(w)
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    res = run_gpu(moe, w, li, extra_rows=3, combine_variant=0, combine_order=1)
+    assert_parity(res, d, out_ref, w, extra_rows=3)
 
 
 def test_non_default_stream_and_reuse(moe, oracle_mod):
