@@ -154,13 +154,19 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int consumer_warps = (blockDim.x >> 5) - 1;
 
-  // Units of this CTA: a contiguous range starting at u0, or (STRIDED) all
-  // pieces of tokens blockIdx.x + m * gridDim.x.
+  // Units of this CTA: a contiguous range starting at u0; or (STRIDED) all
+  // pieces of tokens blockIdx.x + m * G for the R = T / G full rounds, then a
+  // contiguous share, starting at remainder unit v0, of the (T - R*G) * P units
+  // left over, so that no CTA gets a whole token more than another.
   const int64_t G = gridDim.x;
-  int64_t u0, n;
+  const int64_t R = p.T / G;
+  int64_t u0 = 0, n = 0, strided_units = 0, v0 = 0;
   if constexpr (STRIDED) {
-    u0 = static_cast<int64_t>(blockIdx.x) * P;
-    n = (p.T > blockIdx.x ? (p.T - blockIdx.x + G - 1) / G : 0) * P;
+    strided_units = R * P;
+    const int64_t rest = (p.T - R * G) * P;
+    const int64_t q = rest / G, rem = rest % G;
+    v0 = blockIdx.x * q + (blockIdx.x < rem ? blockIdx.x : rem);
+    n = strided_units + q + (blockIdx.x < rem ? 1 : 0);
   } else {
     const int64_t units = static_cast<int64_t>(p.T) * P;
     const int64_t q = units / G, rem = units % G;
@@ -170,9 +176,16 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
   // (token, piece) of the CTA's i-th unit.
   auto unit_at = [&](int64_t i, int64_t& t, int& j) {
     if constexpr (STRIDED) {
-      const int64_t m = i / P;
-      j = static_cast<int>(i - m * P);
-      t = blockIdx.x + m * G;
+      if (i < strided_units) {
+        const int64_t m = i / P;
+        j = static_cast<int>(i - m * P);
+        t = blockIdx.x + m * G;
+      } else {
+        const int64_t v = v0 + (i - strided_units);
+        const int64_t tr = v / P;
+        j = static_cast<int>(v - tr * P);
+        t = R * G + tr;
+      }
     } else {
       const int64_t u = u0 + i;
       t = u / P;
@@ -202,7 +215,9 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
     int64_t t_cur = -1;
     int row = -1, next_row = -1;
     if (n > 0 && lane < K) {
-      const int64_t t0 = STRIDED ? static_cast<int64_t>(blockIdx.x) : u0 / P;
+      int64_t t0;
+      int j0;
+      unit_at(0, t0, j0);
       next_row = p.slot_row[t0 * K + lane];
     }
     bool ok = true;
@@ -216,8 +231,14 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
         row = next_row;
         // Prefetch the next token's rows while this one is in flight.
         if constexpr (STRIDED) {
-          const int64_t tn = t + G;
-          if (lane < K && tn < p.T) next_row = p.slot_row[tn * K + lane];
+          // This CTA's pieces of token t are consecutive from piece j on.
+          const int64_t i_next = i + (P - j);
+          if (i_next < n) {
+            int64_t tn;
+            int jn;
+            unit_at(i_next, tn, jn);
+            if (lane < K) next_row = p.slot_row[tn * K + lane];
+          }
         } else {
           const int64_t tn = t + 1;
           if (lane < K && tn * P < u0 + n) next_row = p.slot_row[tn * K + lane];

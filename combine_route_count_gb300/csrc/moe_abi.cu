@@ -788,14 +788,14 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
     cl.variant = combine_variant_of(ctx);
     cl.grid = 0;
     if (cl.variant == moe::kCombineBulk) {
-      // Many tokens per CTA (at least 16 at two CTAs per SM): the CTAs take
-      // tokens in a strided order and pieces of up to 4 KiB, else a contiguous
-      // range and pieces of up to 2 KiB.  Measured on GB300: Kimi-sized layers
-      // 700 -> 682 us and the worst case 352 -> 345 us with the former;
-      // DeepSeek-sized layers (13.5 tokens per CTA) are fastest with the latter.
-      const bool many = static_cast<int64_t>(c.num_tokens) >= int64_t{32} * grid_sms(ctx);
+      // By default the CTAs take tokens in the strided order (the leftover
+      // tokens split evenly by pieces) with pieces of up to 4 KiB; measured on
+      // GB300 against a contiguous range with 2 KiB pieces: DeepSeek-sized
+      // layers 169.6 -> 167.6 us, Kimi-sized 700 -> 680 us, the worst case
+      // 352 -> 344 us.  (The strided order with 2 KiB pieces was slower.)
+      const bool strided = ctx->combine_order != 0;
       cl.shape = moe::combine_bulk_shape(c.hidden, c.top_k, ctx->combine_stages, ctx->combine_piece_bytes,
-                                         ctx->max_smem_optin, many ? 4096 : 2048);
+                                         ctx->max_smem_optin, strided ? 4096 : 2048);
       cl.shape.hints = ctx->cache_hints;
       cl.shape.drop_unit = ctx->test_drop_unit;
       const size_t smem = moe::combine_bulk_smem_bytes(cl.shape, c.top_k);
@@ -807,7 +807,7 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
       int64_t grid = static_cast<int64_t>(grid_sms(ctx)) * per_sm;
       if (grid > units) grid = units;
       cl.grid = static_cast<int>(grid);
-      cl.shape.strided = ctx->combine_order >= 0 ? ctx->combine_order : (many ? 1 : 0);
+      cl.shape.strided = strided ? 1 : 0;
     }
     if (moe::launch_combine(cp, cl, static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ECUDA;
   }

@@ -263,8 +263,8 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               (default: 0 for K >= 4, else 1)
  *   MOE_OPT_COMBINE_STAGES      bulk: stages per CTA, 2..8, 0 = automatic
  *   MOE_OPT_COMBINE_PIECE_BYTES bulk: bytes of a row per unit, 0 = automatic
- *                               (equal pieces of at most 4 KiB when T >= 32 x
- *                               SMs, else of at most 2 KiB)
+ *                               (equal pieces of at most 4 KiB, or 2 KiB with
+ *                               MOE_OPT_COMBINE_ORDER 0)
  *   MOE_OPT_COMBINE_CTAS_PER_SM bulk: 0 = as many as fit, else 1..32 */
 #define MOE_OPT_COMBINE_VARIANT 8
 #define MOE_OPT_COMBINE_STAGES 9
@@ -308,12 +308,14 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               Only the bulk combine variant honours it. */
 #define MOE_OPT_TEST_DROP_COMBINE_UNIT 16
 /*   MOE_OPT_COMBINE_ORDER       bulk combine: which tokens a CTA takes; 0 = one
- *                               contiguous range of (token, piece) units, 1 =
- *                               tokens b, b+G, b+2G, ... of G CTAs, so that the
- *                               gathered rows being read at any moment lie
- *                               close together in each expert's region; -1 =
- *                               automatic (default: 1 when T >= 32 x SMs,
- *                               i.e. at least 16 tokens per CTA, else 0) */
+ *                               contiguous range of (token, piece) units (and
+ *                               automatic pieces of up to 2 KiB); 1 or -1
+ *                               (default) = tokens b, b+G, b+2G, ... of G CTAs
+ *                               for the T/G full rounds, the leftover tokens'
+ *                               units split evenly, so that the gathered rows
+ *                               being read at any moment lie close together in
+ *                               each expert's region (automatic pieces of up
+ *                               to 4 KiB) */
 #define MOE_OPT_COMBINE_ORDER 17
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
