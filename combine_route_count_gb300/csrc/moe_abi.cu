@@ -127,6 +127,7 @@ struct moe_ctx {
   int max_sms;  // MOE_OPT_MAX_SMS: 0 = every SM
   int64_t test_drop_unit;  // MOE_OPT_TEST_DROP_COMBINE_UNIT (-1: off)
   int combine_order;       // MOE_OPT_COMBINE_ORDER
+  int fp8_order;           // MOE_OPT_FP8_ORDER
   int max_smem_optin;
   int l2_bytes;
   int phase;
@@ -251,6 +252,10 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->combine_variant = -1;  // automatic
   c->test_drop_unit = -1;
   c->combine_order = -1;  // automatic
+  // fp8 pack in the strided token order (measured on GB300: DeepSeek-sized
+  // fp8 layer 141.4 -> 139.0 us, Kimi-sized 545 -> 543 us, Mixtral-sized
+  // unchanged).
+  c->fp8_order = 1;
   // Largest cluster of route_cluster CTAs this device can schedule for this
   // configuration (16, else 8, 4, 2, 1), or none.
   for (int maxc = moe::kMaxClusterCtas; maxc >= 1; maxc /= 2) {
@@ -364,6 +369,10 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       if (value < -1 || value > 1) return MOE_EINVAL;
       ctx->combine_order = static_cast<int>(value);
       return MOE_OK;
+    case MOE_OPT_FP8_ORDER:
+      if (value < 0 || value > 1) return MOE_EINVAL;
+      ctx->fp8_order = static_cast<int>(value);
+      return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       if (value < 0 || value > 3) return MOE_EINVAL;
       if (value == 3 && ctx->cluster_ctas == 0) return MOE_EINVAL;
@@ -427,6 +436,9 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
       return MOE_OK;
     case MOE_OPT_COMBINE_ORDER:
       *value = ctx->combine_order;
+      return MOE_OK;
+    case MOE_OPT_FP8_ORDER:
+      *value = ctx->fp8_order;
       return MOE_OK;
     default:
       return MOE_EINVAL;
@@ -728,7 +740,8 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
     if (per_sm < 1) per_sm = 1;
     int64_t grid = static_cast<int64_t>(grid_sms(ctx)) * per_sm;
     if (grid > c.num_tokens) grid = c.num_tokens;
-    if (moe::launch_dispatch_pack_fp8(fp, static_cast<int>(grid), stages, ctx->pdl != 0, s) != cudaSuccess)
+    if (moe::launch_dispatch_pack_fp8(fp, static_cast<int>(grid), stages, ctx->pdl != 0, ctx->fp8_order == 1, s) !=
+        cudaSuccess)
       return MOE_ECUDA;
   }
   ctx->phase = kDispatched;

@@ -113,7 +113,9 @@ struct PackFp8Params {
 };
 size_t pack_fp8_smem_bytes(int stages, int H);
 int pack_fp8_max_stages();
-cudaError_t launch_dispatch_pack_fp8(const PackFp8Params& p, int grid, int stages, bool pdl, cudaStream_t stream);
+// strided: CTA b packs tokens b, b+grid, ...; else one contiguous token range.
+cudaError_t launch_dispatch_pack_fp8(const PackFp8Params& p, int grid, int stages, bool pdl, bool strided,
+                                     cudaStream_t stream);
 
 // ---- combine: out[t] = bf16(sum_k w[t,k] * y[slot_row[t,k]]) -----------------
 struct CombineParams {

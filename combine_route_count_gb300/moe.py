@@ -33,6 +33,7 @@ MOE_OPT_PACK_STORE_DEPTH = 14
 MOE_OPT_MAX_SMS = 15
 MOE_OPT_TEST_DROP_COMBINE_UNIT = 16
 MOE_OPT_COMBINE_ORDER = 17
+MOE_OPT_FP8_ORDER = 18
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.
@@ -310,7 +311,8 @@ class MoELayer:
                  "combine_piece_bytes": MOE_OPT_COMBINE_PIECE_BYTES,
                  "combine_ctas_per_sm": MOE_OPT_COMBINE_CTAS_PER_SM, "pack_prefetch": MOE_OPT_PACK_PREFETCH,
                  "cache_hints": MOE_OPT_CACHE_HINTS, "pack_store_depth": MOE_OPT_PACK_STORE_DEPTH,
-                 "max_sms": MOE_OPT_MAX_SMS, "combine_order": MOE_OPT_COMBINE_ORDER}
+                 "max_sms": MOE_OPT_MAX_SMS, "combine_order": MOE_OPT_COMBINE_ORDER,
+                 "fp8_order": MOE_OPT_FP8_ORDER}
         for k, v in options.items():
             moe_ctx_set_option(self.ctx, names[k], int(v))
 

@@ -317,6 +317,11 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               each expert's region (automatic pieces of up
  *                               to 4 KiB) */
 #define MOE_OPT_COMBINE_ORDER 17
+/*   MOE_OPT_FP8_ORDER           fp8 pack: which tokens a CTA takes; 0 = one
+ *                               contiguous range, 1 = tokens b, b+G, b+2G, ...
+ *                               of G CTAs (default: their destination rows lie
+ *                               close together in each expert's region) */
+#define MOE_OPT_FP8_ORDER 18
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
 /* ---- Dispatch without any device allocation ------------------------------

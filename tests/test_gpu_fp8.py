@@ -95,6 +95,21 @@ def test_fp8_edge_shapes(moe, oracle_mod, shape, route_variant):
     check(run_fp8(moe, w, li, route_variant=route_variant), oracle_mod, w, li)
 
 
+@pytest.mark.parametrize("name", ["tiny", "mixtral", "deepseek"])
+def test_fp8_contiguous_token_order(moe, oracle_mod, name):
+    w = gen.BY_NAME[name]
+    li = gen.make_inputs(w)
+    check(run_fp8(moe, w, li, fp8_order=0), oracle_mod, w, li)
+
+
+@pytest.mark.parametrize("shape", FP8_EDGE, ids=["x".join(map(str, s)) for s in FP8_EDGE])
+def test_fp8_contiguous_edge_shapes(moe, oracle_mod, shape):
+    T, H, K, E, N = shape
+    w = gen.custom("fp8edge", T=T, H=H, K=K, E=E, N=N, seed_index=23)
+    li = gen.make_inputs(w)
+    check(run_fp8(moe, w, li, fp8_order=0), oracle_mod, w, li)
+
+
 def test_fp8_routing_error_writes_nothing(moe):
     w = gen.custom("fp8bad", T=64, H=256, K=2, E=8, N=2, seed_index=19)
     li = gen.make_inputs(w)
