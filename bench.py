@@ -565,6 +565,16 @@ def run_e2e(args, w, li, layer, stream, dev):
     steps = max(4, min(args.steps, 40))
     run(4)
     torch.cuda.synchronize(dev)
+    # The host link on this machine, measured alone with the same copies: the
+    # floor the end-to-end step cannot beat (uploads dominate it).
+    l0 = torch.cuda.Event(enable_timing=True)
+    l1 = torch.cuda.Event(enable_timing=True)
+    l0.record(s_up)
+    for _ in range(4):
+        upload(0)
+    l1.record(s_up)
+    torch.cuda.synchronize(dev)
+    h2d_gbs = 4 * h2d / (l0.elapsed_time(l1) * 1e-3) / 1e9
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(s_up)
@@ -579,7 +589,8 @@ def run_e2e(args, w, li, layer, stream, dev):
         raise RuntimeError("device reported an error in the end-to-end pass")
     ok = bool(torch.equal(hout, bufs[(steps - 1) % 2]["out"].cpu()))
     return {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "pipelined": True, "out_matches_device": ok}
+            "steps": steps, "pipelined": True, "out_matches_device": ok,
+            "host_link_h2d_gbs": round(h2d_gbs, 1), "h2d_floor_us": round(h2d / h2d_gbs / 1e3, 1)}
 
 
 def run_overlap(args):

@@ -71,7 +71,7 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // work on a window of consecutive tokens and their destination rows lie close
 // together in each expert's region; otherwise one contiguous token range.
 template <int KMAX, bool STRIDED>
-__global__ void __launch_bounds__(32 + kConsumers) dispatch_pack_fp8_kernel(PackFp8Params p, int stages) {
+__global__ void __launch_bounds__(32 + kConsumers, KMAX <= 4 ? 8 : 1) dispatch_pack_fp8_kernel(PackFp8Params p, int stages) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxFp8Stages;
@@ -81,11 +81,11 @@ __global__ void __launch_bounds__(32 + kConsumers) dispatch_pack_fp8_kernel(Pack
   const int nblk = H / 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int64_t G = gridDim.x;
-  const int64_t q = p.T / G, rem = p.T % G;
+  const int64_t q = p.T / gridDim.x, rem = p.T % gridDim.x;
   const int64_t t0 = STRIDED ? static_cast<int64_t>(blockIdx.x) : blockIdx.x * q + (blockIdx.x < rem ? blockIdx.x : rem);
   const int64_t n = q + (blockIdx.x < rem ? 1 : 0);
-  const int64_t dt = STRIDED ? G : 1;  // token step between a CTA's consecutive tokens
+  // token step between a CTA's consecutive tokens
+  const int dt = STRIDED ? static_cast<int>(gridDim.x) : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -100,15 +100,15 @@ __global__ void __launch_bounds__(32 + kConsumers) dispatch_pack_fp8_kernel(Pack
     // ---------------- producer ----------------
     if (lane == 0) {
       bool ok = true;
-      for (int64_t i = 0; i < n; ++i) {
+      int64_t t = t0;
+      for (int64_t i = 0; i < n; ++i, t += dt) {
         const int s = static_cast<int>(i % stages);
         if (i >= stages && !wait_parity(&empty[s], static_cast<uint32_t>(((i / stages) - 1) & 1))) {
           ok = false;
           break;
         }
         ptx::mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(row_bytes));
-        ptx::bulk_g2s(stage_buf + s * row_bytes, p.x + (t0 + i * dt) * row_bytes, static_cast<uint32_t>(row_bytes),
-                      &full[s]);
+        ptx::bulk_g2s(stage_buf + s * row_bytes, p.x + t * row_bytes, static_cast<uint32_t>(row_bytes), &full[s]);
       }
       if (!ok) atomicCAS(p.error_word, MOE_OK, MOE_ETIMEDOUT);
     }
@@ -121,9 +121,9 @@ __global__ void __launch_bounds__(32 + kConsumers) dispatch_pack_fp8_kernel(Pack
   const int chunks = H / 16;
   int next_row = -1;
   if (n > 0 && lane < K) next_row = p.slot_row[t0 * K + lane];
-  for (int64_t i = 0; i < n; ++i) {
+  int64_t t = t0;
+  for (int64_t i = 0; i < n; ++i, t += dt) {
     const int s = static_cast<int>(i % stages);
-    const int64_t t = t0 + i * dt;
     const int my_row = next_row;
     if (i + 1 < n && lane < K) next_row = p.slot_row[(t + dt) * K + lane];
     const bool arrived = wait_parity(&full[s], static_cast<uint32_t>((i / stages) & 1));
@@ -185,12 +185,21 @@ __global__ void __launch_bounds__(32 + kConsumers) dispatch_pack_fp8_kernel(Pack
 }
 
 template <int KMAX>
-cudaError_t launch_fp8_k(const PackFp8Params& p, int grid, int stages, bool pdl, bool strided, cudaStream_t stream) {
+cudaError_t launch_fp8_k(const PackFp8Params& p, int sms, int per_sm, int stages, bool pdl, bool strided,
+                         cudaStream_t stream) {
   auto* kern = strided ? dispatch_pack_fp8_kernel<KMAX, true> : dispatch_pack_fp8_kernel<KMAX, false>;
   const size_t smem = pack_fp8_smem_bytes(stages, p.H);
   cudaError_t err = set_kernel_limits(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
-  return launch_kernel(kern, dim3(grid), dim3(32 + kConsumers), smem, stream, pdl, p, stages);
+  // A persistent grid larger than what can be resident runs a second wave:
+  // never ask for more CTAs per SM than the registers and shared memory allow.
+  const int resident = resident_ctas_per_sm(reinterpret_cast<const void*>(kern), 32 + kConsumers, smem);
+  if (resident > 0 && per_sm > resident) per_sm = resident;
+  if (per_sm < 1) per_sm = 1;
+  int64_t grid = static_cast<int64_t>(sms) * per_sm;
+  if (grid > p.T) grid = p.T;
+  if (grid < 1) grid = 1;
+  return launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(32 + kConsumers), smem, stream, pdl, p, stages);
 }
 
 }  // namespace
@@ -201,14 +210,14 @@ size_t pack_fp8_smem_bytes(int stages, int H) {
 
 int pack_fp8_max_stages() { return kMaxFp8Stages; }
 
-cudaError_t launch_dispatch_pack_fp8(const PackFp8Params& p, int grid, int stages, bool pdl, bool strided,
+cudaError_t launch_dispatch_pack_fp8(const PackFp8Params& p, int sms, int per_sm, int stages, bool pdl, bool strided,
                                      cudaStream_t stream) {
   if (stages < 2) stages = 2;
   if (stages > kMaxFp8Stages) stages = kMaxFp8Stages;
-  if (p.K <= 2) return launch_fp8_k<2>(p, grid, stages, pdl, strided, stream);
-  if (p.K <= 4) return launch_fp8_k<4>(p, grid, stages, pdl, strided, stream);
-  if (p.K <= 8) return launch_fp8_k<8>(p, grid, stages, pdl, strided, stream);
-  return launch_fp8_k<16>(p, grid, stages, pdl, strided, stream);
+  if (p.K <= 2) return launch_fp8_k<2>(p, sms, per_sm, stages, pdl, strided, stream);
+  if (p.K <= 4) return launch_fp8_k<4>(p, sms, per_sm, stages, pdl, strided, stream);
+  if (p.K <= 8) return launch_fp8_k<8>(p, sms, per_sm, stages, pdl, strided, stream);
+  return launch_fp8_k<16>(p, sms, per_sm, stages, pdl, strided, stream);
 }
 
 }  // namespace moe

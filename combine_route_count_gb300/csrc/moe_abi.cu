@@ -19,6 +19,7 @@
 #include <map>
 #include <mutex>
 #include <new>
+#include <tuple>
 #include <utility>
 
 #include "moe.h"
@@ -61,6 +62,20 @@ cudaError_t set_kernel_limits(const void* kernel, size_t bytes, bool nonportable
     entry.second = true;
   }
   return cudaSuccess;
+}
+
+int resident_ctas_per_sm(const void* kernel, int threads, size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, size_t>, int> known;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = known.find({dev, kernel, threads, smem});
+  if (it != known.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) return 0;
+  known[{dev, kernel, threads, smem}] = n;
+  return n;
 }
 
 }  // namespace moe
@@ -738,9 +753,7 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
     const int want = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : (few_dest ? 8 : 3);
     if (per_sm > want) per_sm = want;
     if (per_sm < 1) per_sm = 1;
-    int64_t grid = static_cast<int64_t>(grid_sms(ctx)) * per_sm;
-    if (grid > c.num_tokens) grid = c.num_tokens;
-    if (moe::launch_dispatch_pack_fp8(fp, static_cast<int>(grid), stages, ctx->pdl != 0, ctx->fp8_order == 1, s) !=
+    if (moe::launch_dispatch_pack_fp8(fp, grid_sms(ctx), per_sm, stages, ctx->pdl != 0, ctx->fp8_order == 1, s) !=
         cudaSuccess)
       return MOE_ECUDA;
   }

@@ -113,8 +113,10 @@ struct PackFp8Params {
 };
 size_t pack_fp8_smem_bytes(int stages, int H);
 int pack_fp8_max_stages();
-// strided: CTA b packs tokens b, b+grid, ...; else one contiguous token range.
-cudaError_t launch_dispatch_pack_fp8(const PackFp8Params& p, int grid, int stages, bool pdl, bool strided,
+// Persistent grid of up to sms x per_sm CTAs (fewer if fewer can be resident
+// or T is smaller); strided: CTA b packs tokens b, b+grid, ...; else one
+// contiguous token range.
+cudaError_t launch_dispatch_pack_fp8(const PackFp8Params& p, int sms, int per_sm, int stages, bool pdl, bool strided,
                                      cudaStream_t stream);
 
 // ---- combine: out[t] = bf16(sum_k w[t,k] * y[slot_row[t,k]]) -----------------
@@ -179,6 +181,10 @@ cudaError_t launch_combine_two_level(const TwoLevelParams& p, bool pdl, cudaStre
 // (kernel, device) pair pays the runtime call once; later launches only look
 // the pair up.
 cudaError_t set_kernel_limits(const void* kernel, size_t bytes, bool nonportable_cluster = false);
+
+// CTAs of `kernel` that can be resident on one SM with this block size and
+// dynamic shared memory (0 if the query fails); cached per device.
+int resident_ctas_per_sm(const void* kernel, int threads, size_t smem);
 
 // Launch helper: plain or programmatic-dependent launch with cudaLaunchKernelEx.
 template <typename... KArgs, typename... Args>
