@@ -89,10 +89,11 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) combine_kernel(CombinePa
 
 // ---- bulk variant: a producer warp gathers with the TMA engine ---------------
 //
-// Work unit = (token t, column piece j of the row); CTA b takes a contiguous
-// range of units, so the K rows of one token serve its P consecutive pieces
-// and the next token's slot_row entries are fetched while the current token
-// is in flight.  Stage s holds the K gathered row pieces (K * piece bytes):
+// Work unit = (token t, column piece j of the row).  CTA b takes every piece
+// of tokens b, b+G, b+2G, ... (or, as an option, a contiguous range of
+// units), so the K rows of one token serve its consecutive pieces and the
+// next token's slot_row entries are fetched while the current token is in
+// flight.  Stage s holds the K gathered row pieces (K * piece bytes):
 //   producer (warp 0): waits until stage s is free, lane 0 posts the expected
 //     bytes on full[s], lanes k < K each bulk-load row slot_row[t,k]'s piece;
 //   consumers (warps 1..): wait on full[s], each thread reads its 16-byte
