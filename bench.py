@@ -444,7 +444,43 @@ def run_gpu(args):
                        f"the layer's step time minus that (alone_us: between its own events); "
                        f"{n_attr} calls per phase",
     }
-    if comb_us >= disp_us:
+    # Kernel level: the pack and the combine kernel each between two CUDA
+    # events that the library records on this stream right around its launch
+    # (MOE_OPT_KERNEL_EVENTS), one layer at a time.
+    kernel_us = None
+    if args.dispatch == "direct" and args.combine == "receiver":
+        timer = moe.MoELayer(T, H, K, E, N, device=dev, kernel_events=1)
+        pk, cb = [], []
+        for i in range(min(args.steps, 200) + 3):
+            s = sets[i % len(sets)]
+            dispatch(s, timer)
+            timer.dispatch_recv(stream)
+            timer.combine_send(s["y"], stream)
+            combine(s, timer)
+            a, b = timer.kernel_times()
+            if i >= 3:
+                pk.append(a)
+                cb.append(b)
+        if timer.get_error(stream) != moe.MOE_OK:
+            raise RuntimeError("device reported an error in the kernel timing pass")
+        timer.close()
+        row_out = H * 2 if args.payload == "bf16" else H + (H // 128) * 4
+        pack_bytes = T * H * 2 + rows * row_out + rows * 4
+        comb_bytes = rows * H * 2 + T * H * 2 + rows * 8
+        kernel_us = {"pack": statistics.mean(pk) * 1e3, "combine": statistics.mean(cb) * 1e3}
+        kernels["dispatch_pack_kernel"] = {"us": round(kernel_us["pack"], 2), "bytes": pack_bytes,
+                                           "gbs": round(pack_bytes / kernel_us["pack"] / 1e3, 1),
+                                           "timing": f"events around the kernel launch, {len(pk)} layers"}
+        kernels["combine_kernel"] = {"us": round(kernel_us["combine"], 2), "bytes": comb_bytes,
+                                     "gbs": round(comb_bytes / kernel_us["combine"] / 1e3, 1),
+                                     "timing": f"events around the kernel launch, {len(cb)} layers"}
+    if kernel_us is not None:
+        if kernel_us["combine"] >= kernel_us["pack"]:
+            dom, dom_us, dom_bytes, dom_kernel = "combine", kernel_us["combine"], comb_bytes, "combine"
+        else:
+            dom, dom_us, dom_bytes = "dispatch_pack", kernel_us["pack"], pack_bytes
+            dom_kernel = "dispatch_pack" if args.payload == "bf16" else "dispatch_pack_fp8"
+    elif comb_us >= disp_us:
         dom, dom_us, dom_bytes = "combine", comb_us, ab["combine"]
         dom_kernel = "combine" if args.combine == "receiver" else "combine_two_level"
     else:
@@ -453,7 +489,9 @@ def run_gpu(args):
     achieved = dom_bytes / dom_us / 1e3
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": committed_traffic(dom_kernel, w.name),
-                "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"}
+                "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                "timing": "kernel duration between CUDA events recorded around its launch" if kernel_us
+                          else "phase time (see kernels.attribution)"}
 
     e2e = None
     if not args.no_e2e and args.payload == "bf16" and args.combine == "receiver" and args.dispatch == "direct":

@@ -143,6 +143,10 @@ struct moe_ctx {
   int64_t test_drop_unit;  // MOE_OPT_TEST_DROP_COMBINE_UNIT (-1: off)
   int combine_order;       // MOE_OPT_COMBINE_ORDER
   int fp8_order;           // MOE_OPT_FP8_ORDER
+  int kernel_events;       // MOE_OPT_KERNEL_EVENTS
+  bool events_created;
+  cudaEvent_t ev[4];       // before/after the pack kernel, before/after the combine kernel
+  bool pack_timed, combine_timed;
   int max_smem_optin;
   int l2_bytes;
   int phase;
@@ -299,6 +303,8 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
 }
 
 MOE_API int moe_ctx_destroy(moe_ctx* ctx) {
+  if (ctx && ctx->events_created)
+    for (cudaEvent_t e : ctx->ev) cudaEventDestroy(e);
   delete ctx;
   return MOE_OK;
 }
@@ -388,6 +394,19 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       if (value < 0 || value > 1) return MOE_EINVAL;
       ctx->fp8_order = static_cast<int>(value);
       return MOE_OK;
+    case MOE_OPT_KERNEL_EVENTS:
+      if (value < 0 || value > 1) return MOE_EINVAL;
+      if (value == 1 && !ctx->events_created) {
+        for (int i = 0; i < 4; ++i) {
+          if (cudaEventCreate(&ctx->ev[i]) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(ctx->ev[j]);
+            return MOE_ECUDA;
+          }
+        }
+        ctx->events_created = true;
+      }
+      ctx->kernel_events = static_cast<int>(value);
+      return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       if (value < 0 || value > 3) return MOE_EINVAL;
       if (value == 3 && ctx->cluster_ctas == 0) return MOE_EINVAL;
@@ -454,6 +473,9 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
       return MOE_OK;
     case MOE_OPT_FP8_ORDER:
       *value = ctx->fp8_order;
+      return MOE_OK;
+    case MOE_OPT_KERNEL_EVENTS:
+      *value = ctx->kernel_events;
       return MOE_OK;
     default:
       return MOE_EINVAL;
@@ -653,8 +675,12 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
   if (rrc != MOE_OK) return rrc;
 
   if (c.num_tokens > 0) {
+    const bool timed = ctx->kernel_events != 0;
+    if (timed && cudaEventRecord(ctx->ev[0], s) != cudaSuccess) return MOE_ECUDA;
     const int prc = enqueue_pack(ctx, x, expert_x, ctx->slot_row, c.num_tokens, c.top_k, ctx->pdl != 0, true, -1, s);
     if (prc != MOE_OK) return prc;
+    if (timed && cudaEventRecord(ctx->ev[1], s) != cudaSuccess) return MOE_ECUDA;
+    ctx->pack_timed = timed;
   }
   ctx->phase = kDispatched;
   return MOE_OK;
@@ -753,9 +779,13 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
     const int want = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : (few_dest ? 8 : 3);
     if (per_sm > want) per_sm = want;
     if (per_sm < 1) per_sm = 1;
+    const bool timed = ctx->kernel_events != 0;
+    if (timed && cudaEventRecord(ctx->ev[0], s) != cudaSuccess) return MOE_ECUDA;
     if (moe::launch_dispatch_pack_fp8(fp, grid_sms(ctx), per_sm, stages, ctx->pdl != 0, ctx->fp8_order == 1, s) !=
         cudaSuccess)
       return MOE_ECUDA;
+    if (timed && cudaEventRecord(ctx->ev[1], s) != cudaSuccess) return MOE_ECUDA;
+    ctx->pack_timed = timed;
   }
   ctx->phase = kDispatched;
   return MOE_OK;
@@ -835,7 +865,12 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
       cl.grid = static_cast<int>(grid);
       cl.shape.strided = strided ? 1 : 0;
     }
-    if (moe::launch_combine(cp, cl, static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ECUDA;
+    const bool timed = ctx->kernel_events != 0;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (timed && cudaEventRecord(ctx->ev[2], cs) != cudaSuccess) return MOE_ECUDA;
+    if (moe::launch_combine(cp, cl, cs) != cudaSuccess) return MOE_ECUDA;
+    if (timed && cudaEventRecord(ctx->ev[3], cs) != cudaSuccess) return MOE_ECUDA;
+    ctx->combine_timed = timed;
   }
   ctx->expert_y = nullptr;
   ctx->phase = kIdle;
@@ -882,6 +917,21 @@ MOE_API int moe_combine_recv_two_level(moe_ctx* ctx, const float* topk_w, void* 
   }
   ctx->expert_y = nullptr;
   ctx->phase = kIdle;
+  return MOE_OK;
+}
+
+MOE_API int moe_kernel_times(moe_ctx* ctx, float* pack_ms, float* combine_ms) {
+  if (!ctx || !pack_ms || !combine_ms) return MOE_EINVAL;
+  *pack_ms = -1.0f;
+  *combine_ms = -1.0f;
+  if (ctx->pack_timed) {
+    if (cudaEventSynchronize(ctx->ev[1]) != cudaSuccess) return MOE_ECUDA;
+    if (cudaEventElapsedTime(pack_ms, ctx->ev[0], ctx->ev[1]) != cudaSuccess) return MOE_ECUDA;
+  }
+  if (ctx->combine_timed) {
+    if (cudaEventSynchronize(ctx->ev[3]) != cudaSuccess) return MOE_ECUDA;
+    if (cudaEventElapsedTime(combine_ms, ctx->ev[2], ctx->ev[3]) != cudaSuccess) return MOE_ECUDA;
+  }
   return MOE_OK;
 }
 

@@ -34,6 +34,7 @@ MOE_OPT_MAX_SMS = 15
 MOE_OPT_TEST_DROP_COMBINE_UNIT = 16
 MOE_OPT_COMBINE_ORDER = 17
 MOE_OPT_FP8_ORDER = 18
+MOE_OPT_KERNEL_EVENTS = 19
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.
@@ -41,7 +42,7 @@ EXPORTS = ("moe_validate_config", "moe_workspace_bytes", "moe_recv_bound_rows", 
            "moe_ctx_destroy", "moe_ctx_set_option", "moe_ctx_get_option", "moe_dispatch_send", "moe_dispatch_recv",
            "moe_combine_send", "moe_combine_recv", "moe_get_error", "moe_strerror",
            "moe_dispatch_send_noalloc", "moe_dispatch_send_fp8", "moe_combine_recv_two_level", "moe_partial_rows",
-           "moe_dispatch_send_staged")
+           "moe_dispatch_send_staged", "moe_kernel_times")
 
 
 class moe_config(ctypes.Structure):
@@ -92,6 +93,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_combine_recv": ([P, P, P, P], I),
         "moe_combine_recv_two_level": ([P, P, P, I64, P, P], I),
         "moe_partial_rows": ([C, ctypes.POINTER(ctypes.c_int64)], I),
+        "moe_kernel_times": ([P, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)], I),
         "moe_get_error": ([P, P], I),
         "moe_strerror": ([I], ctypes.c_char_p),
     }
@@ -215,6 +217,13 @@ def moe_partial_rows(cfg: moe_config) -> int:
     return int(v.value)
 
 
+def moe_kernel_times(ctx: int):
+    """(pack_ms, combine_ms) of the last kernels timed with MOE_OPT_KERNEL_EVENTS (-1: not timed)."""
+    a, b = ctypes.c_float(0), ctypes.c_float(0)
+    _check(load_library().moe_kernel_times(ctx, ctypes.byref(a), ctypes.byref(b)), "moe_kernel_times")
+    return float(a.value), float(b.value)
+
+
 def moe_get_error(ctx: int, stream: Any = None) -> int:
     return int(load_library().moe_get_error(ctx, _stream(stream)))
 
@@ -312,7 +321,7 @@ class MoELayer:
                  "combine_ctas_per_sm": MOE_OPT_COMBINE_CTAS_PER_SM, "pack_prefetch": MOE_OPT_PACK_PREFETCH,
                  "cache_hints": MOE_OPT_CACHE_HINTS, "pack_store_depth": MOE_OPT_PACK_STORE_DEPTH,
                  "max_sms": MOE_OPT_MAX_SMS, "combine_order": MOE_OPT_COMBINE_ORDER,
-                 "fp8_order": MOE_OPT_FP8_ORDER}
+                 "fp8_order": MOE_OPT_FP8_ORDER, "kernel_events": MOE_OPT_KERNEL_EVENTS}
         for k, v in options.items():
             moe_ctx_set_option(self.ctx, names[k], int(v))
 
@@ -367,6 +376,9 @@ class MoELayer:
 
     def partial_rows(self) -> int:
         return moe_partial_rows(self.cfg)
+
+    def kernel_times(self):
+        return moe_kernel_times(self.ctx)
 
     def get_error(self, stream: Any = None) -> int:
         return moe_get_error(self.ctx, stream)

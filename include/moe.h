@@ -322,7 +322,21 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               of G CTAs (default: their destination rows lie
  *                               close together in each expert's region) */
 #define MOE_OPT_FP8_ORDER 18
+/*   MOE_OPT_KERNEL_EVENTS       1 = record CUDA events on the caller's stream
+ *                               right before and after the pack kernel of
+ *                               moe_dispatch_send / moe_dispatch_send_fp8 and
+ *                               the combine kernel of moe_combine_recv, for
+ *                               moe_kernel_times (diagnostics: the events keep
+ *                               those kernels from overlapping the kernel
+ *                               before them); 0 = off (default) */
+#define MOE_OPT_KERNEL_EVENTS 19
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
+
+/* Durations, in milliseconds, of the pack kernel and the combine kernel last
+ * enqueued with MOE_OPT_KERNEL_EVENTS on (-1 for one that was not timed);
+ * waits for those events to complete.  MOE_EINVAL for null pointers,
+ * MOE_ECUDA if an event query fails. */
+int moe_kernel_times(moe_ctx* ctx, float* pack_ms, float* combine_ms);
 
 /* ---- Dispatch without any device allocation ------------------------------
  * The pages have no counterpart to this call; it exists for callers that

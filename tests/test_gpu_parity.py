@@ -363,3 +363,23 @@ def test_repeat_runs_are_byte_identical(moe):
         again = run_gpu(moe, w, li)
         for k in ("expert_x", "out", "slot_row", "row_src", "expert_offsets", "src_offsets"):
             assert np.array_equal(first[k], again[k]), k
+
+
+def test_kernel_events_time_both_kernels_and_keep_results(moe, oracle_mod):
+    w = gen.custom("timed", T=1024, H=2048, K=8, E=64, N=8, router="uniform_random", seed_index=83)
+    li = gen.make_inputs(w)
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    res = run_gpu(moe, w, li, kernel_events=1)
+    assert_parity(res, d, out_ref, w)
+    layer = moe.MoELayer(w.T, w.H, w.K, w.E, w.N)
+    assert layer.kernel_times() == (-1.0, -1.0)  # nothing timed yet
+    layer.set_option(moe.MOE_OPT_KERNEL_EVENTS, 1)
+    x, idx, wt, y = (_dev(li.x.view(np.int16)), _dev(li.topk_idx), _dev(li.topk_w), _dev(li.y.view(np.int16)))
+    ex = torch.zeros((w.T * w.K, w.H), dtype=torch.int16, device="cuda")
+    out = torch.zeros((w.T, w.H), dtype=torch.int16, device="cuda")
+    layer.layer(x, idx, wt, ex, y, out)
+    pack_ms, comb_ms = layer.kernel_times()
+    assert 0.0 < pack_ms < 100.0 and 0.0 < comb_ms < 100.0
+    assert layer.get_error() == 0
+    with pytest.raises(moe.MoEError):
+        layer.set_option(moe.MOE_OPT_KERNEL_EVENTS, 2)
