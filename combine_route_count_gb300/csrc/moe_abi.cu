@@ -261,7 +261,7 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->plan_w = reinterpret_cast<float*>(c->ws + l.plan_w);
   c->plan_mask = reinterpret_cast<int32_t*>(c->ws + l.plan_mask);
   c->pack_variant = moe::kPackBulk;
-  c->pack_stages = 0;  // automatic: about 100 KiB of stages per CTA
+  c->pack_stages = 0;  // automatic: about 200 KiB of stages per SM
   c->pack_prefetch = 2;
   c->cache_hints = moe::kHintPackLoads | moe::kHintPackStores | moe::kHintCombineLoads;
   c->pack_piece_bytes = 0;
@@ -611,7 +611,8 @@ int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, const int32_t* table,
   pl.variant = variant >= 0 ? variant : ctx->pack_variant;
   pl.stages = ctx->pack_stages;
   if (pl.stages <= 0) {
-    // About 100 KiB of stages per CTA (two CTAs per SM), 2..16 stages.
+    // About 200 KiB of stages per SM split over the automatic CTAs per SM
+    // (two for K >= 4: ~100 KiB each; three otherwise), 2..16 stages.
     pl.stages = static_cast<int>((200 * 1024) / pack_ctas_auto(K) / pp.piece_bytes);
     if (pl.stages > 16) pl.stages = 16;
     if (pl.stages < 2) pl.stages = 2;
