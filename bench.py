@@ -600,7 +600,7 @@ def run_e2e(args, w, li, layer, stream, dev):
                 hout.copy_(B["out"], non_blocking=True)
             down_ev[b].record(s_down)
 
-    steps = max(4, min(args.steps, 40))
+    steps = max(4, min(args.steps, 100))
     run(4)
     torch.cuda.synchronize(dev)
     # The host link on this machine, measured alone with the same copies: the
