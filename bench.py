@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--buffer-sets", type=int, default=2)
-    ap.add_argument("--payload", choices=["bf16", "fp8"], default="bf16",
+    ap.add_argument("--payload", choices=["bf16", "fp8", "fp8q"], default="bf16",
                     help="dispatch payload: bf16 rows, or block-scaled fp8 rows (moe_dispatch_send_fp8)")
     ap.add_argument("--dispatch", choices=["direct", "staged"], default="direct",
                     help="rows straight to their grouped position (moe_dispatch_send), or through per-peer "
@@ -70,7 +70,8 @@ def algorithmic_bytes(w, payload="bf16", partial_rows=None, staged=False):
     row = H * 2
     pairs = T * K
     out_row = row if payload == "bf16" else H + (H // 128) * 4
-    dispatch = T * row + pairs * out_row
+    in_row = H + (H // 128) * 4 if payload == "fp8q" else row  # fp8q: tokens arrive already quantised
+    dispatch = T * in_row + pairs * out_row
     if staged:
         dispatch += 2 * pairs * row
     dispatch_meta = 2 * pairs * 4 + 2 * pairs * 4 + pairs * 4 + (3 * E + E * N + N + 2) * 4
@@ -278,8 +279,17 @@ def run_gpu(args):
         idx0 = torch.from_numpy(li.topk_idx).to(dev)
         w0 = torch.from_numpy(li.topk_w).to(dev)
         y0 = torch.from_numpy(li.y.view(np.int16)).to(dev)
+        if args.payload == "fp8q":
+            # Already-quantised tokens: any byte pattern is a valid payload for
+            # the copy, so seeded random codes and scales stand in for them.
+            g = torch.Generator(device=dev)
+            g.manual_seed(1234)
+            xq0 = torch.randint(0, 256, (T, H), generator=g, device=dev, dtype=torch.uint8)
+            xs0 = torch.rand((T, H // 128), generator=g, device=dev, dtype=torch.float32) + 1e-3
         for _ in range(args.buffer_sets):
             sets.append(dict(x=x0.clone(), idx=idx0.clone(), w=w0.clone(), y=y0.clone(),
+                             xq=xq0.clone() if args.payload == "fp8q" else None,
+                             xs=xs0.clone() if args.payload == "fp8q" else None,
                              expert_x=torch.empty((rows, H), dtype=torch.int16, device=dev)
                              if args.payload == "bf16" else torch.empty((rows, H), dtype=torch.uint8, device=dev),
                              expert_scales=None if args.payload == "bf16"
@@ -301,6 +311,8 @@ def run_gpu(args):
             lay.dispatch_send_staged(s["x"], s["idx"], s["send"], s["expert_x"], stream)
         elif args.payload == "bf16":
             lay.dispatch_send(s["x"], s["idx"], s["expert_x"], stream)
+        elif args.payload == "fp8q":
+            lay.dispatch_send_quantized(s["xq"], s["xs"], s["idx"], s["expert_x"], s["expert_scales"], stream)
         else:
             lay.dispatch_send_fp8(s["x"], s["idx"], s["expert_x"], s["expert_scales"], stream)
 
@@ -448,7 +460,7 @@ def run_gpu(args):
     # events that the library records on this stream right around its launch
     # (MOE_OPT_KERNEL_EVENTS), one layer at a time.
     kernel_us = None
-    if args.dispatch == "direct" and args.combine == "receiver":
+    if args.dispatch == "direct" and args.combine == "receiver" and args.payload != "fp8q":
         timer = moe.MoELayer(T, H, K, E, N, device=dev, kernel_events=1)
         pk, cb = [], []
         for i in range(min(args.steps, 200) + 3):
@@ -506,7 +518,9 @@ def run_gpu(args):
             "metric": METRIC, "value": round(us_layer, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if args.payload == "bf16" else "fp8-e4m3 dispatch / bf16 combine", "data": "synthetic",
+            "dtype": {"bf16": "bf16", "fp8": "fp8-e4m3 dispatch (quantised in the pack) / bf16 combine",
+                      "fp8q": "fp8-e4m3 dispatch (tokens already quantised) / bf16 combine"}[args.payload],
+            "data": "synthetic",
             "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": f"inputs > L2: {ab['total'] / 1e6:.0f} MB moved per layer, "
@@ -535,7 +549,7 @@ def run_gpu(args):
             "e2e": e2e,
             "clocks": clk,
             "gpu_launches": (layer.kernels_per_layer() + (args.combine == "two_level")
-                             + 2 * (args.dispatch == "staged")) * args.steps,
+                             + 2 * (args.dispatch == "staged") + (args.payload == "fp8q")) * args.steps,
         }
         print(json.dumps(line), flush=True)
     layer.close()

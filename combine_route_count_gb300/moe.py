@@ -42,7 +42,7 @@ EXPORTS = ("moe_validate_config", "moe_workspace_bytes", "moe_recv_bound_rows", 
            "moe_ctx_destroy", "moe_ctx_set_option", "moe_ctx_get_option", "moe_dispatch_send", "moe_dispatch_recv",
            "moe_combine_send", "moe_combine_recv", "moe_get_error", "moe_strerror",
            "moe_dispatch_send_noalloc", "moe_dispatch_send_fp8", "moe_combine_recv_two_level", "moe_partial_rows",
-           "moe_dispatch_send_staged", "moe_kernel_times")
+           "moe_dispatch_send_staged", "moe_kernel_times", "moe_dispatch_send_quantized")
 
 
 class moe_config(ctypes.Structure):
@@ -87,6 +87,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_ctx_get_option": ([P, I, ctypes.POINTER(ctypes.c_int64)], I),
         "moe_dispatch_send": ([P, P, P, P, I64, P], I),
         "moe_dispatch_send_fp8": ([P, P, P, P, P, I64, P], I),
+        "moe_dispatch_send_quantized": ([P, P, P, P, P, P, I64, P], I),
         "moe_dispatch_send_staged": ([P, P, P, P, I64, P, I64, P], I),
         "moe_dispatch_recv": ([P, ctypes.POINTER(moe_dispatch_layout), P], I),
         "moe_combine_send": ([P, P, I64, P], I),
@@ -189,6 +190,13 @@ def moe_dispatch_send_staged(ctx: int, x: Any, topk_idx: Any, send_buf: Any, sen
     _check(load_library().moe_dispatch_send_staged(ctx, _ptr(x), _ptr(topk_idx), _ptr(send_buf), send_rows,
                                                    _ptr(expert_x), expert_x_rows, _stream(stream)),
            "moe_dispatch_send_staged")
+
+
+def moe_dispatch_send_quantized(ctx: int, xq: Any, x_scales: Any, topk_idx: Any, expert_xq: Any, expert_scales: Any,
+                                expert_rows: int, stream: Any = None) -> None:
+    _check(load_library().moe_dispatch_send_quantized(ctx, _ptr(xq), _ptr(x_scales), _ptr(topk_idx), _ptr(expert_xq),
+                                                      _ptr(expert_scales), expert_rows, _stream(stream)),
+           "moe_dispatch_send_quantized")
 
 
 def moe_dispatch_recv(ctx: int, stream: Any = None) -> moe_dispatch_layout:
@@ -358,6 +366,11 @@ class MoELayer:
         """Two-stage dispatch: send_buf bf16 [>= T*K, H] is caller scratch."""
         moe_dispatch_send_staged(self.ctx, x, topk_idx, send_buf, send_buf.shape[0], expert_x, expert_x.shape[0],
                                  stream)
+
+    def dispatch_send_quantized(self, xq, x_scales, topk_idx, expert_xq, expert_scales, stream: Any = None) -> None:
+        """Pre-quantised payload: xq uint8 [T, H], x_scales float32 [T, H/128]."""
+        moe_dispatch_send_quantized(self.ctx, xq, x_scales, topk_idx, expert_xq, expert_scales, expert_xq.shape[0],
+                                    stream)
 
     def dispatch_recv(self, stream: Any = None) -> "DispatchLayout":
         """The dispatch layout; its arrays are torch views into the workspace,

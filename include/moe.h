@@ -146,6 +146,22 @@ int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void
 int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_xq,
                           float* expert_scales, int64_t expert_rows, void* stream);
 
+/* Dispatch, send half, for tokens the caller has already quantised to fp8
+ * (the other reading of "Efficient and portable mixture-of-experts
+ * communication", Dispatch: tokens travel together with their block scaling
+ * factors).  Same routing and row placement as moe_dispatch_send; the E4M3
+ * code rows and their float32 block-scale rows are copied as they are:
+ *   expert_xq[slot_row[t,k]] = xq[t], expert_scales[slot_row[t,k]] = x_scales[t].
+ *   xq             device E4M3 bytes [T, H], 16-byte aligned
+ *   x_scales       device float32 [T, H / MOE_FP8_BLOCK], 16-byte aligned
+ *   expert_xq      device E4M3 bytes [expert_rows, H], 16-byte aligned
+ *   expert_scales  device float32 [expert_rows, H / MOE_FP8_BLOCK], 16-byte aligned
+ *   expert_rows    >= T*K; rows [0, T*K) of both are written
+ * H must be a multiple of 512 (scale rows a multiple of 16 bytes); MOE_EINVAL
+ * otherwise.  Errors and call order as for moe_dispatch_send. */
+int moe_dispatch_send_quantized(moe_ctx* ctx, const void* xq, const float* x_scales, const int32_t* topk_idx,
+                                void* expert_xq, float* expert_scales, int64_t expert_rows, void* stream);
+
 /* Dispatch, send half, two-stage form ("Enabling trillion-parameter models on
  * AWS EFA", dispatch and combine timing: the sender copies tokens into
  * contiguous per-peer send buffers at offsets from the cumulative sum of its
@@ -170,8 +186,8 @@ int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t* topk_id
  * in the grouped layout (the shared-buffer case of "Efficient and portable
  * mixture-of-experts communication", Further improvements), so this enqueues
  * nothing: it fills `layout` with device pointers to the counts, offsets and
- * routing tables.  Valid after moe_dispatch_send, moe_dispatch_send_fp8 or
- * moe_dispatch_send_staged. */
+ * routing tables.  Valid after moe_dispatch_send, moe_dispatch_send_fp8,
+ * moe_dispatch_send_quantized or moe_dispatch_send_staged. */
 int moe_dispatch_recv(moe_ctx* ctx, moe_dispatch_layout* layout, void* stream);
 
 /* Combine, send half: registers the expert outputs, one row per dispatched
