@@ -15,6 +15,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
+# Checked build: every row index read from a routing table is verified against
+# its buffer before use (MOE_ECORRUPT); a separate library and object folder.
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libmoe_checked.so")
 SOURCES = ["route_count.cu", "route_split.cu", "route_cluster.cu", "dispatch_pack.cu", "dispatch_fp8.cu", "dispatch_staged.cu", "combine.cu", "combine_two_level.cu", "moe_abi.cu", "moe_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -35,17 +39,23 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: Optional[List[str]] = None) -> str:
-    """Compile csrc/*.cu into libmoe.so next to this file; returns its path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input() and not extra_flags:
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags: Optional[List[str]] = None,
+          checked: bool = False) -> str:
+    """Compile csrc/*.cu into libmoe.so next to this file (libmoe_checked.so
+    with checked=True); returns its path."""
+    lib = LIB_CHECKED if checked else LIB
+    build_dir = BUILD_CHECKED if checked else BUILD
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input() and not extra_flags:
+        return lib
     nv = nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
                     "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC] + list(extra_flags or [])
+    if checked:
+        flags.append("-DMOE_CHECKED")
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         cmd = [nv] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -56,15 +66,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags: Optional[List
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     libdir = _cuda_lib_dir(nv)
     cmd = [nv] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs + [
         "-Xlinker", f"-rpath,{libdir}", "-L", libdir]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"link of libmoe.so failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

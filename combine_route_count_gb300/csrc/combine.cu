@@ -59,8 +59,10 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) combine_kernel(CombinePa
   for (int k = 0; k < KMAX; ++k) {
     if (k < K) {
       const int r = slots[k];
-      bad |= r < 0;
-      if (r >= 0) v[k] = ptx::ld_stream_v4(p.y + static_cast<int64_t>(r) * row_bytes + c * 16);
+      const bool out_of_range = kChecked && r >= p.y_rows;
+      if (out_of_range) atomicCAS(p.error_word, MOE_OK, MOE_ECORRUPT);
+      bad |= r < 0 || out_of_range;
+      if (r >= 0 && !out_of_range) v[k] = ptx::ld_stream_v4(p.y + static_cast<int64_t>(r) * row_bytes + c * 16);
     }
   }
   if (bad) return;  // routing error reported by route_count: leave out[t] untouched
@@ -255,7 +257,9 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
       // Failure-injection hook (tests only): nothing is posted for this unit,
       // so its consumers' bounded wait runs out and reports MOE_ETIMEDOUT.
       if (DROP && t * P + j == sh.drop_unit) continue;
-      const bool bad = __any_sync(0xffffffffu, lane < K && row < 0);
+      const bool out_of_range = kChecked && lane < K && row >= p.y_rows;
+      if (out_of_range) atomicCAS(p.error_word, MOE_OK, MOE_ECORRUPT);
+      const bool bad = __any_sync(0xffffffffu, lane < K && (row < 0 || out_of_range));
       const uint32_t bytes = piece_len(j);
       if (lane == 0) {
         skip[s] = bad ? 1 : 0;

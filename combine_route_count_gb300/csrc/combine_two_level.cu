@@ -81,6 +81,10 @@ __global__ void __launch_bounds__(kThreads) combine_plan_kernel(TwoLevelParams p
     if (k < K) {
       row[k] = p.slot_row[t * K + k];
       bad |= row[k] < 0;
+      if (kChecked && row[k] >= p.y_rows) {
+        atomicCAS(p.error_word, MOE_OK, MOE_ECORRUPT);
+        bad = 1;
+      }
     }
   }
   if (bad) {

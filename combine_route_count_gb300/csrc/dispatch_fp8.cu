@@ -124,8 +124,12 @@ __global__ void __launch_bounds__(32 + kConsumers, KMAX <= 4 ? 8 : 1) dispatch_p
   int64_t t = t0;
   for (int64_t i = 0; i < n; ++i, t += dt) {
     const int s = static_cast<int>(i % stages);
-    const int my_row = next_row;
+    int my_row = next_row;
     if (i + 1 < n && lane < K) next_row = p.slot_row[(t + dt) * K + lane];
+    if (kChecked && lane < K && my_row >= 0 && my_row >= p.dst_rows) {
+      atomicCAS(p.error_word, MOE_OK, MOE_ECORRUPT);
+      my_row = -1;  // treated like a routing error: the token is skipped
+    }
     const bool arrived = wait_parity(&full[s], static_cast<uint32_t>((i / stages) & 1));
     if (!__all_sync(0xffffffffu, arrived)) {
       if (lane == 0) atomicCAS(p.error_word, MOE_OK, MOE_ETIMEDOUT);

@@ -167,7 +167,12 @@ __global__ void __launch_bounds__(32) dispatch_pack_bulk(PackParams p, int stage
       const uint32_t lines = (piece_bytes(j) + 127) / 128;
       for (uint32_t q = lane; q < lines; q += 32) ptx::l2_priority_normal(src + static_cast<size_t>(q) * 128);
     }
-    if (row >= 0) {
+    int row_ok = row;
+    if (kChecked && row >= 0 && row >= p.dst_rows) {
+      report(p.error_word, MOE_ECORRUPT);
+      row_ok = -1;
+    }
+    if (row_ok >= 0) {
       uint8_t* dst = p.expert_x + static_cast<int64_t>(row) * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes;
       const uint8_t* src = stage_buf + static_cast<size_t>(s) * p.piece_bytes;
       if (hints & kHintPackStores)
@@ -209,7 +214,11 @@ __global__ void __launch_bounds__(256) dispatch_pack_vector(PackParams p) {
   for (int64_t u = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += warps) {
     const int64_t t = u / p.pieces;
     const int j = static_cast<int>(u - t * p.pieces);
-    const int my_row = lane < p.K ? p.slot_row[t * p.K + lane] : -1;
+    int my_row = lane < p.K ? p.slot_row[t * p.K + lane] : -1;
+    if (kChecked && my_row >= 0 && my_row >= p.dst_rows) {
+      report(p.error_word, MOE_ECORRUPT);
+      my_row = -1;
+    }
     const int64_t off = static_cast<int64_t>(j) * p.piece_bytes;
     const int64_t left = p.row_bytes - off;
     const int chunks = static_cast<int>((left < p.piece_bytes ? left : p.piece_bytes) >> 4);

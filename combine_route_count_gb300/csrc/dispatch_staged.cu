@@ -80,6 +80,11 @@ __global__ void __launch_bounds__(kThreads) staged_layout_kernel(StagedLayoutPar
     const int e = p.topk_idx[pair];
     const int g = p.slot_row[pair];
     const int64_t j = base + pre[e] + (g - p.src_offsets[static_cast<int64_t>(e) * p.N + s]);
+    if (kChecked && (j < base || j >= base + n)) {
+      atomicCAS(p.error_word, MOE_OK, MOE_ECORRUPT);
+      p.send_pos[pair] = -1;
+      continue;
+    }
     p.send_pos[pair] = static_cast<int32_t>(j);
     p.send_dest[j] = g;
   }

@@ -595,8 +595,8 @@ namespace {
 // `prefetch` allows the context's L2 prefetch of source rows (which pays
 // while the pack overlaps routing); `variant` < 0 takes the context's pack
 // variant.
-int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, const int32_t* table, int32_t T, int32_t K,
-                 int64_t row_bytes, bool pdl, bool prefetch, int variant, cudaStream_t s) {
+int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, int64_t dst_rows, const int32_t* table, int32_t T,
+                 int32_t K, int64_t row_bytes, bool pdl, bool prefetch, int variant, cudaStream_t s) {
   moe::PackParams pp = {};
   pp.x = static_cast<const uint8_t*>(src);
   pp.expert_x = static_cast<uint8_t*>(dst);
@@ -604,6 +604,7 @@ int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, const int32_t* table,
   pp.error_word = ctx->error_word;
   pp.T = T;
   pp.K = K;
+  pp.dst_rows = dst_rows;
   pp.row_bytes = row_bytes;
   pp.piece_bytes = pack_piece_bytes(ctx, pp.row_bytes);
   pp.pieces = static_cast<int32_t>((pp.row_bytes + pp.piece_bytes - 1) / pp.piece_bytes);
@@ -679,7 +680,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     const bool timed = ctx->kernel_events != 0;
     if (timed && cudaEventRecord(ctx->ev[0], s) != cudaSuccess) return MOE_ECUDA;
     const int64_t row_bytes = static_cast<int64_t>(c.hidden) * 2;
-    const int prc = enqueue_pack(ctx, x, expert_x, ctx->slot_row, c.num_tokens, c.top_k, row_bytes, ctx->pdl != 0,
+    const int prc = enqueue_pack(ctx, x, expert_x, expert_x_rows, ctx->slot_row, c.num_tokens, c.top_k, row_bytes, ctx->pdl != 0,
                                  true, -1, s);
     if (prc != MOE_OK) return prc;
     if (timed && cudaEventRecord(ctx->ev[1], s) != cudaSuccess) return MOE_ECUDA;
@@ -717,10 +718,12 @@ MOE_API int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t*
     sp.K = c.top_k;
     sp.E = c.num_experts;
     sp.N = c.num_ranks;
+    sp.error_word = ctx->error_word;
     if (moe::launch_staged_layout(sp, ctx->pdl != 0, s) != cudaSuccess) return MOE_ECUDA;
     // Stage 1, every source rank: x rows into its per-peer send rows.
     const int64_t row_bytes = static_cast<int64_t>(c.hidden) * 2;
-    int prc = enqueue_pack(ctx, x, send_buf, ctx->send_pos, c.num_tokens, c.top_k, row_bytes, ctx->pdl != 0, true, -1,
+    int prc = enqueue_pack(ctx, x, send_buf, send_rows, ctx->send_pos, c.num_tokens, c.top_k, row_bytes, ctx->pdl != 0,
+                           true, -1,
                            s);
     if (prc != MOE_OK) return prc;
     // Stage 2, every receiver: send rows into the grouped rows.  Its source is
@@ -728,7 +731,8 @@ MOE_API int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t*
     // nothing for an L2 prefetch to overlap.  One destination per row: the
     // 16-byte vector copy is used (measured faster on GB300 than the bulk
     // pipeline, which moves one row piece per stage cycle when K = 1).
-    prc = enqueue_pack(ctx, send_buf, expert_x, ctx->send_dest, static_cast<int32_t>(pairs), 1, row_bytes, false, false,
+    prc = enqueue_pack(ctx, send_buf, expert_x, expert_x_rows, ctx->send_dest, static_cast<int32_t>(pairs), 1, row_bytes,
+                       false, false,
                        moe::kPackVector, s);
     if (prc != MOE_OK) return prc;
   }
@@ -761,10 +765,11 @@ MOE_API int moe_dispatch_send_quantized(moe_ctx* ctx, const void* xq, const floa
     // (H/32 bytes): the 16-byte vector copy moves them with less per-row
     // overhead than the bulk pipeline (measured on GB300: DeepSeek-sized
     // layer 148.0 -> 134.6 us; doing them first was slower, 138.2 us).
-    int prc = enqueue_pack(ctx, xq, expert_xq, ctx->slot_row, c.num_tokens, c.top_k, c.hidden, ctx->pdl != 0, true,
+    int prc = enqueue_pack(ctx, xq, expert_xq, expert_rows, ctx->slot_row, c.num_tokens, c.top_k, c.hidden,
+                           ctx->pdl != 0, true,
                            -1, s);
     if (prc != MOE_OK) return prc;
-    prc = enqueue_pack(ctx, x_scales, expert_scales, ctx->slot_row, c.num_tokens, c.top_k, scale_row_bytes,
+    prc = enqueue_pack(ctx, x_scales, expert_scales, expert_rows, ctx->slot_row, c.num_tokens, c.top_k, scale_row_bytes,
                        ctx->pdl != 0, false, moe::kPackVector, s);
     if (prc != MOE_OK) return prc;
   }
@@ -800,6 +805,7 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
     fp.T = c.num_tokens;
     fp.K = c.top_k;
     fp.H = c.hidden;
+    fp.dst_rows = expert_rows;
     // MOE_OPT_PACK_STAGES / _CTAS_PER_SM apply here too.  Automatic, K >= 4:
     // about 72 KiB of row stages per CTA, three CTAs (12 consumer warps) per
     // SM.  K < 4: each token row carries little write traffic for the
@@ -879,6 +885,7 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
     cp.T = c.num_tokens;
     cp.K = c.top_k;
     cp.H = c.hidden;
+    cp.y_rows = ctx->expert_y_rows;
     cp.error_word = ctx->error_word;
     moe::CombineLaunch cl = {};
     cl.pdl = ctx->pdl != 0;
@@ -953,6 +960,8 @@ MOE_API int moe_combine_recv_two_level(moe_ctx* ctx, const float* topk_w, void* 
     tp.K = c.top_k;
     tp.H = c.hidden;
     tp.N = c.num_ranks;
+    tp.y_rows = ctx->expert_y_rows;
+    tp.error_word = ctx->error_word;
     if (moe::launch_combine_two_level(tp, ctx->pdl != 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return MOE_ECUDA;
   }
@@ -999,6 +1008,8 @@ MOE_API const char* moe_strerror(int status) {
       return "CUDA runtime or launch failure";
     case MOE_EBOUND:
       return "a logical rank would receive more rows than N*T/N*max(K,E/N)";
+    case MOE_ECORRUPT:
+      return "a routing-table entry points outside its buffer (checked build)";
     case MOE_ETIMEDOUT:
       return "a bounded wait inside a kernel gave up";
     default:

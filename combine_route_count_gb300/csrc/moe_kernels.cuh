@@ -10,6 +10,17 @@
 
 namespace moe {
 
+// Checked builds (compiled with -DMOE_CHECKED, libmoe_checked.so) verify every
+// row index read from a routing table against the buffer it addresses before
+// using it; an entry out of range sets MOE_ECORRUPT in the error word and the
+// access is skipped.  In the normal build the checks are constant-false and
+// compile away.
+#ifdef MOE_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
 // ---- route_count: counts, exclusive scan, stable slot ranks (one block) ----
 struct RouteCountParams {
   const int32_t* topk_idx;  // [T, K]
@@ -84,6 +95,7 @@ struct PackParams {
   int64_t row_bytes;        // H * 2, multiple of 16
   int32_t piece_bytes;      // bytes moved per unit (multiple of 16, <= row_bytes)
   int32_t pieces;           // ceil(row_bytes / piece_bytes)
+  int64_t dst_rows;         // rows of expert_x (checked builds verify every table entry against it)
 };
 enum PackVariant { kPackBulk = 0, kPackVector = 1 };
 // L2 eviction hints on the bulk copies (bit flags, MOE_OPT_CACHE_HINTS).
@@ -110,6 +122,7 @@ struct PackFp8Params {
   const int32_t* slot_row;  // [T*K]
   int32_t* error_word;
   int32_t T, K, H;          // H % 128 == 0
+  int64_t dst_rows;         // rows of expert_xq / expert_scales (checked builds)
 };
 size_t pack_fp8_smem_bytes(int stages, int H);
 int pack_fp8_max_stages();
@@ -127,6 +140,7 @@ struct CombineParams {
   uint8_t* out;             // [T, H] bf16
   int32_t* error_word;      // [1] bounded waits report MOE_ETIMEDOUT here
   int32_t T, K, H;
+  int64_t y_rows;           // rows of y (checked builds verify slot_row against it)
 };
 enum CombineVariant { kCombineBulk = 0, kCombineVector = 1 };
 struct BulkCombineShape {
@@ -158,6 +172,7 @@ struct StagedLayoutParams {
   int32_t* send_pos;              // [T*K] send row of pair t*K+k (-1 after a routing error)
   int32_t* send_dest;             // [T*K] grouped row of send row j (-1 after a routing error)
   int32_t T, K, E, N;
+  int32_t* error_word;            // checked builds report MOE_ECORRUPT here
 };
 cudaError_t launch_staged_layout(const StagedLayoutParams& p, bool pdl, cudaStream_t stream);
 
@@ -173,6 +188,8 @@ struct TwoLevelParams {
   float* plan_w;                // [T*K] their weights
   int32_t* plan_mask;           // [T] bit i: sorted slot i ends a rank's group (0: routing error)
   int32_t T, K, H, N;
+  int64_t y_rows;               // rows of y (checked builds)
+  int32_t* error_word;          // checked builds report MOE_ECORRUPT here
 };
 cudaError_t launch_combine_two_level(const TwoLevelParams& p, bool pdl, cudaStream_t stream);
 

@@ -133,6 +133,7 @@ MOE_API int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, cons
   pp.error_word = status;
   pp.T = cfg->num_tokens;
   pp.K = cfg->top_k;
+  pp.dst_rows = expert_x_rows;
   pp.row_bytes = static_cast<int64_t>(cfg->hidden) * 2;
   // Same launch shape as moe_dispatch_send's defaults: pieces of at most
   // 16 KiB, 4 bulk stages, as many CTAs per SM as shared memory allows.

@@ -19,7 +19,7 @@ from typing import Any, Dict, Optional
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe.so")
 
-MOE_OK, MOE_EINVAL, MOE_ESTATE, MOE_EROUTE, MOE_ECUDA, MOE_EBOUND, MOE_ETIMEDOUT = range(7)
+MOE_OK, MOE_EINVAL, MOE_ESTATE, MOE_EROUTE, MOE_ECUDA, MOE_EBOUND, MOE_ETIMEDOUT, MOE_ECORRUPT = range(8)
 MOE_MAX_TOP_K = 16
 MOE_MAX_EXPERTS = 1024
 (MOE_OPT_PACK_VARIANT, MOE_OPT_PACK_STAGES, MOE_OPT_PACK_PIECE_BYTES, MOE_OPT_PACK_CTAS_PER_SM, MOE_OPT_PDL,

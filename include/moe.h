@@ -46,6 +46,7 @@ extern "C" {
 #define MOE_ECUDA 4     /* a CUDA runtime call or a launch failed */
 #define MOE_EBOUND 5    /* device: a rank would receive more than N*T/N*max(K,E/N) rows */
 #define MOE_ETIMEDOUT 6 /* device: a bounded wait inside a kernel gave up */
+#define MOE_ECORRUPT 7  /* device, checked builds only: a routing-table entry points outside its buffer */
 
 /* Limits of this implementation. */
 #define MOE_MAX_TOP_K 16
