@@ -103,9 +103,20 @@ def test_errors_detected_before_any_cuda_call(moe):
 
 
 def test_strerror(moe):
-    for code in range(7):
-        assert moe.moe_strerror(code)
+    for code in range(8):
+        assert moe.moe_strerror(code) != "unknown status"
     assert moe.moe_strerror(99) == "unknown status"
+
+
+def test_status_codes_and_options_match_the_header(moe):
+    """Every MOE_E* status and MOE_OPT_* option the header defines has the
+    same value in the binding."""
+    import re
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    defs = dict(re.findall(r"#define (MOE_(?:OK|E[A-Z]+|OPT_[A-Z0-9_]+)) (-?\d+)", text))
+    assert "MOE_ECORRUPT" in defs and "MOE_OPT_KERNEL_EVENTS" in defs
+    for name, value in defs.items():
+        assert getattr(moe, name) == int(value), name
 
 
 def test_product_path_never_touches_the_oracle():
