@@ -736,6 +736,7 @@ MOE_API int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t*
                        moe::kPackVector, s);
     if (prc != MOE_OK) return prc;
   }
+  ctx->pack_timed = false;  // the event-timed pack is that of moe_dispatch_send(_fp8) only
   ctx->phase = kDispatched;
   return MOE_OK;
 }
@@ -773,6 +774,7 @@ MOE_API int moe_dispatch_send_quantized(moe_ctx* ctx, const void* xq, const floa
                        ctx->pdl != 0, false, moe::kPackVector, s);
     if (prc != MOE_OK) return prc;
   }
+  ctx->pack_timed = false;
   ctx->phase = kDispatched;
   return MOE_OK;
 }
@@ -965,6 +967,7 @@ MOE_API int moe_combine_recv_two_level(moe_ctx* ctx, const float* topk_w, void* 
     if (moe::launch_combine_two_level(tp, ctx->pdl != 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return MOE_ECUDA;
   }
+  ctx->combine_timed = false;  // the event-timed combine is that of moe_combine_recv only
   ctx->expert_y = nullptr;
   ctx->phase = kIdle;
   return MOE_OK;

@@ -104,7 +104,10 @@ int moe_recv_bound_rows(const moe_config* cfg, int64_t* rows);
 /* Creates a context over a caller-owned device workspace of at least
  * moe_workspace_bytes() bytes.  Must be called with the device that owns the
  * workspace current; all later calls must use a stream of that device.
- * The context is not thread-safe: one host thread drives one context. */
+ * The context is not thread-safe: one host thread drives one context.
+ * MOE_EINVAL for a bad configuration, a null, short or misaligned workspace,
+ * a configuration whose routing tables do not fit in shared memory, or when
+ * the host handle cannot be allocated; MOE_ECUDA if a device query fails. */
 int moe_ctx_create(const moe_config* cfg, void* workspace, size_t workspace_bytes, moe_ctx** out);
 
 /* Frees the host handle (not the workspace). NULL is a no-op. */
@@ -349,10 +352,13 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
 #define MOE_OPT_KERNEL_EVENTS 19
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
-/* Durations, in milliseconds, of the pack kernel and the combine kernel last
- * enqueued with MOE_OPT_KERNEL_EVENTS on (-1 for one that was not timed);
- * waits for those events to complete.  MOE_EINVAL for null pointers,
- * MOE_ECUDA if an event query fails. */
+/* Durations, in milliseconds, of the pack kernel of the context's last
+ * dispatch and of the combine kernel of its last combine.  Each is -1 unless
+ * that call was moe_dispatch_send / moe_dispatch_send_fp8 (pack) or
+ * moe_combine_recv (combine) made with MOE_OPT_KERNEL_EVENTS on; the
+ * staged, quantised and two-level variants are not timed.  Waits for the
+ * events to complete.  MOE_EINVAL for null pointers, MOE_ECUDA if an event
+ * query fails. */
 int moe_kernel_times(moe_ctx* ctx, float* pack_ms, float* combine_ms);
 
 /* ---- Dispatch without any device allocation ------------------------------

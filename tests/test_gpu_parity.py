@@ -381,5 +381,15 @@ def test_kernel_events_time_both_kernels_and_keep_results(moe, oracle_mod):
     pack_ms, comb_ms = layer.kernel_times()
     assert 0.0 < pack_ms < 100.0 and 0.0 < comb_ms < 100.0
     assert layer.get_error() == 0
+    # The staged dispatch and the two-level combine are not timed: after them
+    # the times of the earlier layer are no longer reported.
+    send = torch.zeros_like(ex)
+    partial = torch.zeros((layer.partial_rows(), w.H), dtype=torch.int16, device="cuda")
+    layer.dispatch_send_staged(x, idx, send, ex)
+    layer.dispatch_recv()
+    layer.combine_send(y)
+    layer.combine_recv_two_level(wt, partial, out)
+    assert layer.kernel_times() == (-1.0, -1.0)
+    assert layer.get_error() == 0
     with pytest.raises(moe.MoEError):
         layer.set_option(moe.MOE_OPT_KERNEL_EVENTS, 2)
