@@ -307,19 +307,29 @@ class MoELayer:
     """One dispatch+combine context on the current CUDA device.
 
     Allocates the workspace with torch (the library itself allocates no
-    device memory) and exposes the four calls on torch tensors:
+    device memory), or uses the caller's `workspace` (a uint8 CUDA tensor of
+    at least moe_workspace_bytes, 256-byte aligned, e.g. from a pool), and
+    exposes the four calls on torch tensors:
     x bf16 [T, H], topk_idx int32 [T, K], expert_x bf16 [>= T*K, H],
     expert_y bf16 [>= T*K, H], topk_w float32 [T, K], out bf16 [T, H].
     """
 
-    def __init__(self, T: int, H: int, K: int, E: int, N: int, device: Any = None, **options: int):
+    def __init__(self, T: int, H: int, K: int, E: int, N: int, device: Any = None, workspace: Any = None,
+                 **options: int):
         import torch
         self.cfg = make_config(T, H, K, E, N)
         self.T, self.H, self.K, self.E, self.N = T, H, K, E, N
-        self.device = torch.device("cuda") if device is None else torch.device(device)
         nbytes = moe_workspace_bytes(self.cfg)
+        if workspace is not None:
+            if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+                raise MoEError(MOE_EINVAL, "workspace must be a contiguous uint8 CUDA tensor")
+            self.device = workspace.device
+        else:
+            self.device = torch.device("cuda") if device is None else torch.device(device)
         with torch.cuda.device(self.device):
-            self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            if workspace is None:
+                workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            self.workspace = workspace
             self.ctx = moe_ctx_create(self.cfg, self.workspace, self.workspace.numel())
         names = {"pack_variant": MOE_OPT_PACK_VARIANT, "pack_stages": MOE_OPT_PACK_STAGES,
                  "pack_piece_bytes": MOE_OPT_PACK_PIECE_BYTES, "pack_ctas_per_sm": MOE_OPT_PACK_CTAS_PER_SM,
