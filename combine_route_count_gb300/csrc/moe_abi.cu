@@ -90,7 +90,7 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 struct WorkspaceLayout {
   size_t error_word, expert_counts, expert_offsets, src_offsets, rank_offsets, slot_row, row_src, hist, block_err,
-      send_pos, send_dest, plan_row, plan_w, plan_mask, total;
+      send_pos, send_dest, plan_row, plan_w, plan_mask, queue, total;
 };
 
 WorkspaceLayout layout_of(const moe_config& c) {
@@ -125,6 +125,8 @@ WorkspaceLayout layout_of(const moe_config& c) {
   o += align_up(sizeof(float) * pairs);
   l.plan_mask = o;
   o += align_up(sizeof(int32_t) * static_cast<size_t>(c.num_tokens));
+  l.queue = o;  // the bulk pack's unit queue (set to 0 by the routing kernel of every dispatch)
+  o += align_up(sizeof(unsigned long long));
   l.total = o;
   return l;
 }
@@ -166,6 +168,7 @@ struct moe_ctx {
   int32_t* plan_row;
   float* plan_w;
   int32_t* plan_mask;
+  unsigned long long* queue;
   // launch options (MOE_OPT_* in moe.h)
   int pack_variant;
   int pack_stages;
@@ -174,6 +177,7 @@ struct moe_ctx {
   int pack_prefetch;     // 1 = prefetch the CTA's later token rows into L2 before routing completes
   int cache_hints;       // MOE_OPT_CACHE_HINTS bit flags
   int pack_depth;        // MOE_OPT_PACK_STORE_DEPTH (0 = default)
+  int pack_schedule;     // MOE_OPT_PACK_SCHEDULE (-1 = automatic)
   int pdl;
   int route_variant;  // MOE_OPT_ROUTE_VARIANT
   int combine_variant;      // MOE_OPT_COMBINE_VARIANT
@@ -260,6 +264,8 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->plan_row = reinterpret_cast<int32_t*>(c->ws + l.plan_row);
   c->plan_w = reinterpret_cast<float*>(c->ws + l.plan_w);
   c->plan_mask = reinterpret_cast<int32_t*>(c->ws + l.plan_mask);
+  c->queue = reinterpret_cast<unsigned long long*>(c->ws + l.queue);
+  c->pack_schedule = -1;
   c->pack_variant = moe::kPackBulk;
   c->pack_stages = 0;  // automatic: about 200 KiB of stages per SM
   c->pack_prefetch = 2;
@@ -362,6 +368,10 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       if (value < 0 || value > 8) return MOE_EINVAL;
       ctx->pack_depth = static_cast<int>(value);
       return MOE_OK;
+    case MOE_OPT_PACK_SCHEDULE:
+      if (value < -1 || value > 1) return MOE_EINVAL;
+      ctx->pack_schedule = static_cast<int>(value);
+      return MOE_OK;
     case MOE_OPT_COMBINE_VARIANT:
       if (value != -1 && value != moe::kCombineBulk && value != moe::kCombineVector) return MOE_EINVAL;
       ctx->combine_variant = static_cast<int>(value);
@@ -443,6 +453,9 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
       return MOE_OK;
     case MOE_OPT_PACK_STORE_DEPTH:
       *value = ctx->pack_depth;
+      return MOE_OK;
+    case MOE_OPT_PACK_SCHEDULE:
+      *value = ctx->pack_schedule;
       return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       *value = ctx->route_variant != 0 ? ctx->route_variant : (ctx->cluster_ctas > 0 ? 3 : 2);
@@ -537,6 +550,7 @@ int enqueue_routing(moe_ctx* ctx, const int32_t* topk_idx, cudaStream_t s) {
   rp.slot_row = ctx->slot_row;
   rp.row_src = ctx->row_src;
   rp.error_word = ctx->error_word;
+  rp.queue = ctx->queue;
   int vec = 1;
   if (c.top_k % 4 == 0 && aligned(topk_idx, 16)) vec = 4;
   else if (c.top_k % 2 == 0 && aligned(topk_idx, 8)) vec = 2;
@@ -561,6 +575,7 @@ int enqueue_routing(moe_ctx* ctx, const int32_t* topk_idx, cudaStream_t s) {
     cp.slot_row = ctx->slot_row;
     cp.row_src = ctx->row_src;
     cp.error_word = ctx->error_word;
+    cp.queue = ctx->queue;
     if (moe::launch_route_cluster(cp, vec, ctx->cluster_ctas, s) != cudaSuccess) return MOE_ECUDA;
   } else {
     moe::RouteSplitParams sp = {};
@@ -579,6 +594,7 @@ int enqueue_routing(moe_ctx* ctx, const int32_t* topk_idx, cudaStream_t s) {
     sp.error_word = ctx->error_word;
     sp.hist = ctx->hist;
     sp.block_err = ctx->block_err;
+    sp.queue = ctx->queue;
     if (moe::launch_route_split(sp, vec, s) != cudaSuccess) return MOE_ECUDA;
   }
   return MOE_OK;
@@ -592,11 +608,12 @@ namespace {
 // for T source rows of H bf16 each (a table entry < 0 is skipped).  The
 // bulk pack reads its first source rows before waiting on the previous
 // kernel, so `pdl` must be false when src is that kernel's output.
-// `prefetch` allows the context's L2 prefetch of source rows (which pays
-// while the pack overlaps routing); `variant` < 0 takes the context's pack
-// variant.
+// `after_routing` marks the first pack after the routing kernels: it may
+// prefetch source rows into L2 while routing runs (the context's prefetch
+// mode) and claim units from the queue that routing has just reset (the
+// context's schedule); `variant` < 0 takes the context's pack variant.
 int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, int64_t dst_rows, const int32_t* table, int32_t T,
-                 int32_t K, int64_t row_bytes, bool pdl, bool prefetch, int variant, cudaStream_t s) {
+                 int32_t K, int64_t row_bytes, bool pdl, bool after_routing, int variant, cudaStream_t s) {
   moe::PackParams pp = {};
   pp.x = static_cast<const uint8_t*>(src);
   pp.expert_x = static_cast<uint8_t*>(dst);
@@ -627,7 +644,7 @@ int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, int64_t dst_rows, con
       return MOE_EINVAL;
   }
   pl.grid = pack_grid(ctx, pp, pl.variant, pl.stages);
-  pl.prefetch = prefetch ? ctx->pack_prefetch : 0;
+  pl.prefetch = after_routing ? ctx->pack_prefetch : 0;
   pl.prefetch_units = -1;
   if (pl.prefetch == 2) {
     // Evict-last prefetch when every row a CTA still needs after its
@@ -654,6 +671,16 @@ int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, int64_t dst_rows, con
   // 1 GiB (Kimi-sized layers: 3 % faster than with two).
   const int64_t dest_bytes = static_cast<int64_t>(T) * K * pp.row_bytes;
   pl.depth = ctx->pack_depth > 0 ? ctx->pack_depth : (dest_bytes > (int64_t{1} << 30) ? 1 : 2);
+  // Unit queue (bulk pack, first pack after routing): automatic when a CTA
+  // has more than 1.5x its prologue's worth of units.  Measured on GB300:
+  // the DeepSeek-, Kimi- and worst-case-sized layers gain from it; with about
+  // one prologue of units per CTA (Mixtral-sized layers) the claims of all
+  // CTAs at once cost more than the balance gives back.
+  if (after_routing && pl.variant == moe::kPackBulk && ctx->pack_schedule != 0) {
+    const int64_t units = static_cast<int64_t>(T) * pp.pieces;
+    pl.dynamic = ctx->pack_schedule == 1 || 2 * units > 3 * static_cast<int64_t>(pl.stages) * pl.grid;
+    if (pl.dynamic) pp.queue = ctx->queue;
+  }
   if (moe::launch_dispatch_pack(pp, pl, s) != cudaSuccess) return MOE_ECUDA;
   return MOE_OK;
 }

@@ -32,6 +32,7 @@ struct RouteCountParams {
   int32_t* slot_row;        // [T*K]
   int32_t* row_src;         // [T*K]
   int32_t* error_word;      // [1]
+  unsigned long long* queue;  // [1] the bulk pack's unit queue: set to 0 here (may be null)
 };
 constexpr int kRouteThreads = 1024;
 // Dynamic shared memory the kernel needs for E experts.
@@ -53,6 +54,7 @@ struct RouteSplitParams {
   int32_t* slot_row;        // [T*K]
   int32_t* row_src;         // [T*K]
   int32_t* error_word;      // [1]
+  unsigned long long* queue;  // [1] the bulk pack's unit queue: set to 0 here (may be null)
   int32_t* hist;            // [blocks*E] per-chunk expert histograms
   int32_t* block_err;       // [blocks]   per-chunk routing error flags
 };
@@ -77,6 +79,7 @@ struct RouteClusterParams {
   int32_t* slot_row;        // [T*K]
   int32_t* row_src;         // [T*K]
   int32_t* error_word;      // [1]
+  unsigned long long* queue;  // [1] the bulk pack's unit queue: set to 0 here (may be null)
 };
 size_t route_cluster_smem_bytes(int E, int warps, int staged_pairs);
 // Fills chunk/warps/staged/dsmem_group of p for a cluster of `cluster` CTAs.
@@ -96,6 +99,7 @@ struct PackParams {
   int32_t piece_bytes;      // bytes moved per unit (multiple of 16, <= row_bytes)
   int32_t pieces;           // ceil(row_bytes / piece_bytes)
   int64_t dst_rows;         // rows of expert_x (checked builds verify every table entry against it)
+  unsigned long long* queue;  // [1] unit queue of the dynamic schedule, 0 at launch (set by routing)
 };
 enum PackVariant { kPackBulk = 0, kPackVector = 1 };
 // L2 eviction hints on the bulk copies (bit flags, MOE_OPT_CACHE_HINTS).
@@ -109,6 +113,7 @@ struct PackLaunch {
   int hints;      // CacheHints
   int depth;      // bulk: store groups in flight before a stage is refilled (0 = default 1)
   int prefetch_units;  // bulk: units past the prologue each CTA prefetches (-1 = all)
+  bool dynamic;        // bulk: after its first `stages` units a CTA claims units from p.queue
 };
 size_t pack_bulk_smem_bytes(int stages, int piece_bytes);
 cudaError_t prepare_pack(int max_smem_bytes);  // one-time per-device attribute setup

@@ -35,6 +35,7 @@ MOE_OPT_TEST_DROP_COMBINE_UNIT = 16
 MOE_OPT_COMBINE_ORDER = 17
 MOE_OPT_FP8_ORDER = 18
 MOE_OPT_KERNEL_EVENTS = 19
+MOE_OPT_PACK_SCHEDULE = 20
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.
@@ -339,7 +340,8 @@ class MoELayer:
                  "combine_ctas_per_sm": MOE_OPT_COMBINE_CTAS_PER_SM, "pack_prefetch": MOE_OPT_PACK_PREFETCH,
                  "cache_hints": MOE_OPT_CACHE_HINTS, "pack_store_depth": MOE_OPT_PACK_STORE_DEPTH,
                  "max_sms": MOE_OPT_MAX_SMS, "combine_order": MOE_OPT_COMBINE_ORDER,
-                 "fp8_order": MOE_OPT_FP8_ORDER, "kernel_events": MOE_OPT_KERNEL_EVENTS}
+                 "fp8_order": MOE_OPT_FP8_ORDER, "kernel_events": MOE_OPT_KERNEL_EVENTS,
+                 "pack_schedule": MOE_OPT_PACK_SCHEDULE}
         for k, v in options.items():
             moe_ctx_set_option(self.ctx, names[k], int(v))
 

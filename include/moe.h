@@ -92,8 +92,9 @@ int moe_validate_config(const moe_config* cfg);
 
 /* Device workspace (bytes, a multiple of 256) that one context needs: counts,
  * offsets, slot_row, row_src, the error word, the send tables of
- * moe_dispatch_send_staged and the plan of moe_combine_recv_two_level.  Allocate it 256-byte
- * aligned; its contents need no initialisation. */
+ * moe_dispatch_send_staged, the plan of moe_combine_recv_two_level and the
+ * pack's unit queue.  Allocate it 256-byte aligned; its contents need no
+ * initialisation (every dispatch writes what it later reads). */
 int moe_workspace_bytes(const moe_config* cfg, size_t* bytes);
 
 /* The receive bound of "Enabling trillion-parameter models on AWS EFA"
@@ -350,6 +351,18 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               those kernels from overlapping the kernel
  *                               before them); 0 = off (default) */
 #define MOE_OPT_KERNEL_EVENTS 19
+/*   MOE_OPT_PACK_SCHEDULE       bulk pack of moe_dispatch_send and of the
+ *                               first stage of the staged and quantised
+ *                               dispatches: 0 = static (CTA b copies units b,
+ *                               b+G, b+2G, ... of the G CTAs); 1 = unit queue
+ *                               (each CTA takes its first `stages` units
+ *                               statically, then claims units in increasing
+ *                               order from a counter in the workspace that the
+ *                               routing kernel resets, so faster CTAs take
+ *                               more); -1 = automatic (default: the queue when
+ *                               a CTA has more than 1.5x its first `stages`
+ *                               units).  Results are identical. */
+#define MOE_OPT_PACK_SCHEDULE 20
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
 /* Durations, in milliseconds, of the pack kernel of the context's last

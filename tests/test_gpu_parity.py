@@ -167,6 +167,14 @@ PACK_OPTIONS = [
     dict(combine_variant=0, combine_order=1),
     dict(combine_variant=0, combine_order=1, combine_piece_bytes=2048 + 16, combine_stages=3, combine_ctas_per_sm=3),
     dict(combine_variant=0, combine_order=0),
+    dict(pack_schedule=0),
+    dict(pack_schedule=1),
+    dict(pack_schedule=1, pack_stages=2, pack_store_depth=1),
+    dict(pack_schedule=1, pack_stages=16, pack_store_depth=8, pack_ctas_per_sm=1),
+    dict(pack_schedule=1, pack_piece_bytes=2048, pack_prefetch=2),
+    dict(pack_schedule=1, pack_prefetch=0, cache_hints=0, pdl=0),
+    dict(pack_schedule=1, route_variant=1),
+    dict(pack_schedule=1, route_variant=2),
 ]
 
 
@@ -224,6 +232,44 @@ def test_empty_layer(moe):
     assert lay["expert_offsets"].cpu().tolist() == [0] * 9
     assert lay["src_offsets"].cpu().numpy().tolist() == [[0, 0]] * 8
     assert _intact(big, 0)
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=["x".join(map(str, s[:5])) for s in EDGE])
+def test_edge_shapes_pack_queue(moe, oracle_mod, shape):
+    """The bulk pack with its unit queue forced on, at every edge shape."""
+    T, H, K, E, N, router = shape
+    w = gen.custom("edge", T=T, H=H, K=K, E=E, N=N, router=router, seed_index=17)
+    li = gen.make_inputs(w)
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    res = run_gpu(moe, w, li, extra_rows=2, pack_schedule=1, pack_variant=0)
+    assert_parity(res, d, out_ref, w, extra_rows=2)
+
+
+def test_pack_queue_is_reset_every_layer(moe, oracle_mod):
+    """Layers with different routings on one context, the queue forced on:
+    each layer's routing resets the queue (a stale count would leave units
+    uncopied), also across a routing error and with each routing variant."""
+    T, H, K, E, N = 2048, 1024, 8, 64, 8
+    layer = moe.MoELayer(T, H, K, E, N, pack_schedule=1)
+    ex = torch.empty((T * K, H), dtype=torch.int16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    for n, route in enumerate([0, 0, 1, 2, 3, 0]):
+        w = gen.custom("queue", T=T, H=H, K=K, E=E, N=N, router="uniform_random", seed_index=40 + n)
+        li = gen.make_inputs(w)
+        d, out_ref = oracle_of(oracle_mod, w, li)
+        x, idx, wt, y = (_dev(li.x.view(np.int16)), _dev(li.topk_idx), _dev(li.topk_w), _dev(li.y.view(np.int16)))
+        layer.set_option(moe.MOE_OPT_ROUTE_VARIANT, route)
+        if n == 3:
+            bad = li.topk_idx.copy()
+            bad[7, 3] = bad[7, 2]  # a repeated expert: nothing is copied, the queue is still consumed
+            bad_d = _dev(bad)
+            layer.layer(x, bad_d, wt, ex, y, out)
+            assert layer.get_error() == moe.MOE_EROUTE
+        lay = layer.layer(x, idx, wt, ex, y, out)
+        assert layer.get_error() == 0
+        assert np.array_equal(lay["slot_row"].cpu().numpy(), d.slot_row)
+        assert np.array_equal(ex.cpu().numpy().view(np.uint16), d.expert_x), n
+        assert np.array_equal(out.cpu().numpy().view(np.uint16), out_ref), n
 
 
 @pytest.mark.parametrize("shape", EDGE, ids=["x".join(map(str, s[:5])) for s in EDGE])

@@ -70,22 +70,24 @@ def check(res, oracle_mod, w, li, xq, xs):
     assert np.array_equal(res["s"].view(np.uint16), ds.expert_x)
 
 
+@pytest.mark.parametrize("pack_schedule", [-1, 1])
 @pytest.mark.parametrize("name", ["mixtral", "deepseek", "kimi", "worst"])
-def test_quantized_named_workloads(moe, oracle_mod, name):
+def test_quantized_named_workloads(moe, oracle_mod, name, pack_schedule):
     w = gen.BY_NAME[name]
     li = gen.make_inputs(w, with_y=False)
     xq, xs = payload(w, 89)
-    check(run(moe, w, li, xq, xs), oracle_mod, w, li, xq, xs)
+    check(run(moe, w, li, xq, xs, pack_schedule=pack_schedule), oracle_mod, w, li, xq, xs)
 
 
+@pytest.mark.parametrize("pack_schedule", [0, 1])
 @pytest.mark.parametrize("shape", [(1, 512, 1, 1, 1), (1000, 1024, 16, 64, 4), (96, 512, 3, 12, 3)],
                          ids=["1x512x1", "1000x1024x16", "96x512x3"])
-def test_quantized_edge_shapes(moe, oracle_mod, shape):
+def test_quantized_edge_shapes(moe, oracle_mod, shape, pack_schedule):
     T, H, K, E, N = shape
     w = gen.custom("q", T=T, H=H, K=K, E=E, N=N, seed_index=97)
     li = gen.make_inputs(w, with_y=False)
     xq, xs = payload(w, 101)
-    check(run(moe, w, li, xq, xs), oracle_mod, w, li, xq, xs)
+    check(run(moe, w, li, xq, xs, pack_schedule=pack_schedule), oracle_mod, w, li, xq, xs)
 
 
 def test_quantized_routing_error_writes_nothing(moe):

@@ -86,13 +86,14 @@ STAGED_EDGE = [
 ]
 
 
+@pytest.mark.parametrize("pack_schedule", [-1, 0, 1])
 @pytest.mark.parametrize("route_variant", [0, 1, 2])
 @pytest.mark.parametrize("shape", STAGED_EDGE, ids=["x".join(map(str, s)) for s in STAGED_EDGE])
-def test_staged_edge_shapes(moe, oracle_mod, shape, route_variant):
+def test_staged_edge_shapes(moe, oracle_mod, shape, route_variant, pack_schedule):
     T, H, K, E, N = shape
     w = gen.custom("stagededge", T=T, H=H, K=K, E=E, N=N, seed_index=67)
     li = gen.make_inputs(w)
-    check(run_staged(moe, w, li, route_variant=route_variant), oracle_mod, w, li)
+    check(run_staged(moe, w, li, route_variant=route_variant, pack_schedule=pack_schedule), oracle_mod, w, li)
 
 
 def test_staged_empty_layer(moe):
