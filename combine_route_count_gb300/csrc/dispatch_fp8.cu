@@ -31,6 +31,8 @@ namespace {
 constexpr int kConsumers = 128;
 constexpr int kMaxFp8Stages = 8;
 constexpr int kFp8BarBytes = 256;
+// Queue variant: mbarriers, stage_tok[8] and stage_rows[8][16] before the stages.
+constexpr int kFp8QueueHeaderBytes = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ unsigned long long now_ns() {
@@ -65,6 +67,58 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Consumer warps (thread c0 = 0..127 of them): quantise the bf16 row in shared
+// memory and store its codes and block scales to the K destination rows; lane
+// k of every consumer warp holds destination row k in my_row.
+template <int KMAX>
+__device__ __forceinline__ void quantize_row(const PackFp8Params& p, const uint8_t* row, int my_row, int c0,
+                                             int chunks, int nblk) {
+  const int K = p.K, H = p.H;
+  // Warp-uniform trip count: every lane reaches the shuffles below; lanes
+  // past the end of the row work on zeros and store nothing.
+  for (int cb = 0; cb < chunks; cb += kConsumers) {
+    const int c = cb + c0;
+    const bool act = c < chunks;
+    const uint4 a = act ? lds128(row + c * 32) : make_uint4(0, 0, 0, 0);
+    const uint4 b = act ? lds128(row + c * 32 + 16) : make_uint4(0, 0, 0, 0);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float f[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16);
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    // The 8 lanes of one 128-element block are 8 consecutive lanes.
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    const float inv = __fdiv_rn(1.0f, scale);
+    uint4 out;
+    uint32_t* o = &out.x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = e4m3x2(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
+      const uint32_t hi = e4m3x2(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
+      o[j] = lo | (hi << 16);
+    }
+    const int blk = c >> 3;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (k < K) {
+        const int64_t dst = static_cast<int64_t>(__shfl_sync(0xffffffffu, my_row, k));
+        if (act) {
+          ptx::st_v4(p.expert_xq + dst * H + static_cast<int64_t>(c) * 16, out);
+          if ((c & 7) == 0) p.expert_scales[dst * nblk + blk] = scale;
+        }
+      }
+    }
+  }
 }
 
 // STRIDED: CTA b takes tokens b, b+G, b+2G, ... (G CTAs), so that the CTAs
@@ -139,50 +193,124 @@ __global__ void __launch_bounds__(32 + kConsumers, KMAX <= 4 ? 8 : 1) dispatch_p
     const bool skip = __any_sync(0xffffffffu, lane < K && my_row < 0);
     const uint8_t* row = stage_buf + s * row_bytes;
     if (!skip) {
-      // Warp-uniform trip count: every lane reaches the shuffles below; lanes
-      // past the end of the row work on zeros and store nothing.
-      for (int cb = 0; cb < chunks; cb += kConsumers) {
-        const int c = cb + c0;
-        const bool act = c < chunks;
-        const uint4 a = act ? lds128(row + c * 32) : make_uint4(0, 0, 0, 0);
-        const uint4 b = act ? lds128(row + c * 32 + 16) : make_uint4(0, 0, 0, 0);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        float f[16];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          f[2 * j] = __uint_as_float(w[j] << 16);
-          f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-        // The 8 lanes of one 128-element block are 8 consecutive lanes.
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-        const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        const float inv = __fdiv_rn(1.0f, scale);
-        uint4 out;
-        uint32_t* o = &out.x;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t lo = e4m3x2(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
-          const uint32_t hi = e4m3x2(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
-          o[j] = lo | (hi << 16);
-        }
-        const int blk = c >> 3;
-#pragma unroll
-        for (int k = 0; k < KMAX; ++k) {
-          if (k < K) {
-            const int64_t dst = static_cast<int64_t>(__shfl_sync(0xffffffffu, my_row, k));
-            if (act) {
-              ptx::st_v4(p.expert_xq + dst * H + static_cast<int64_t>(c) * 16, out);
-              if ((c & 7) == 0) p.expert_scales[dst * nblk + blk] = scale;
-            }
-          }
-        }
+      quantize_row<KMAX>(p, row, my_row, c0, chunks, nblk);
+    }
+    __syncwarp();
+    if (lane == 0) arrive(&empty[s]);
+  }
+}
+
+// Token queue: CTA b quantises tokens b, b+G, ..., b+(stages-1)G (its
+// prologue, loaded while routing runs), then claims tokens stages*G, ... in
+// increasing order from a counter that the routing kernel resets, so that
+// CTAs that progress faster take more tokens.  The producer warp publishes
+// each stage's token and its K destination rows in shared memory; full[s]
+// counts two arrivals per phase (the load's expect_tx, then "rows written"),
+// and token -1 with two plain arrivals ends a CTA's sequence.
+template <int KMAX>
+__global__ void __launch_bounds__(32 + kConsumers, KMAX <= 4 ? 8 : 1)
+    dispatch_pack_fp8_queue_kernel(PackFp8Params p, int stages) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxFp8Stages;
+  int64_t* stage_tok = reinterpret_cast<int64_t*>(empty + kMaxFp8Stages);      // [kMaxFp8Stages]
+  int32_t* stage_rows = reinterpret_cast<int32_t*>(stage_tok + kMaxFp8Stages);  // [kMaxFp8Stages][MOE_MAX_TOP_K]
+  uint8_t* stage_buf = smem + kFp8QueueHeaderBytes;
+  const int K = p.K, H = p.H;
+  const int64_t row_bytes = static_cast<int64_t>(H) * 2;
+  const int nblk = H / 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t G = gridDim.x, T = p.T;
+  const int64_t static_end = static_cast<int64_t>(stages) * G;
+  const int64_t static_tok = T < static_end ? T : static_end;
+  const int64_t nstatic = static_tok > blockIdx.x ? (static_tok - blockIdx.x + G - 1) / G : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      ptx::mbar_init(&full[s], 2);
+      ptx::mbar_init(&empty[s], kConsumers / 32);
+    }
+    ptx::mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    auto load = [&](int s, int64_t t) {
+      ptx::mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(row_bytes));
+      ptx::bulk_g2s(stage_buf + s * row_bytes, p.x + t * row_bytes, static_cast<uint32_t>(row_bytes), &full[s]);
+    };
+    if (lane == 0) {
+      for (int i = 0; i < stages; ++i) {
+        const int64_t t = i < nstatic ? blockIdx.x + i * G : -1;
+        stage_tok[i] = t;
+        if (t >= 0) load(i, t);
       }
     }
+    __syncwarp();
+    ptx::wait_prerequisites();  // slot_row, and the queue reset, come from routing
+    bool claiming = T > static_end;
+    unsigned long long claim = 0;
+    if (lane == 0 && claiming) claim = atomicAdd(p.queue, 1ull);
+    for (int64_t i = 0;; ++i) {
+      const int s = static_cast<int>(i % stages);
+      int64_t t;
+      if (i < stages) {
+        t = stage_tok[s];
+      } else {
+        // The stage is free once the consumers of sequence i - stages are done.
+        const bool freed = wait_parity(&empty[s], static_cast<uint32_t>(((i / stages) - 1) & 1));
+        if (!__all_sync(0xffffffffu, freed)) {
+          if (lane == 0) atomicCAS(p.error_word, MOE_OK, MOE_ETIMEDOUT);
+          break;
+        }
+        t = -1;
+        if (lane == 0) {
+          if (claiming) {
+            const int64_t c = static_end + static_cast<int64_t>(claim);
+            if (c < T) {
+              t = c;
+              claim = atomicAdd(p.queue, 1ull);
+            } else {
+              claiming = false;
+            }
+          }
+          stage_tok[s] = t;
+          if (t >= 0) load(s, t);
+        }
+        t = __shfl_sync(0xffffffffu, t, 0);
+      }
+      // The token's destination rows, published with the stage.
+      if (lane < K) stage_rows[s * MOE_MAX_TOP_K + lane] = t >= 0 ? p.slot_row[t * K + lane] : -1;
+      __syncwarp();
+      if (lane == 0) {
+        if (t < 0) arrive(&full[s]);  // no load: its arrival too
+        arrive(&full[s]);
+      }
+      if (t < 0) break;
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int c0 = threadIdx.x - 32;
+  const int chunks = H / 16;
+  for (int64_t i = 0;; ++i) {
+    const int s = static_cast<int>(i % stages);
+    const bool arrived = wait_parity(&full[s], static_cast<uint32_t>((i / stages) & 1));
+    if (!__all_sync(0xffffffffu, arrived)) {
+      if (lane == 0) atomicCAS(p.error_word, MOE_OK, MOE_ETIMEDOUT);
+      break;
+    }
+    if (stage_tok[s] < 0) break;
+    int my_row = lane < K ? stage_rows[s * MOE_MAX_TOP_K + lane] : -1;
+    if (kChecked && lane < K && my_row >= 0 && my_row >= p.dst_rows) {
+      atomicCAS(p.error_word, MOE_OK, MOE_ECORRUPT);
+      my_row = -1;
+    }
+    // Routing error: slot_row is -1 everywhere, nothing is written.
+    if (!__any_sync(0xffffffffu, lane < K && my_row < 0))
+      quantize_row<KMAX>(p, stage_buf + s * row_bytes, my_row, c0, chunks, nblk);
     __syncwarp();
     if (lane == 0) arrive(&empty[s]);
   }
@@ -191,8 +319,10 @@ __global__ void __launch_bounds__(32 + kConsumers, KMAX <= 4 ? 8 : 1) dispatch_p
 template <int KMAX>
 cudaError_t launch_fp8_k(const PackFp8Params& p, int sms, int per_sm, int stages, bool pdl, bool strided,
                          cudaStream_t stream) {
-  auto* kern = strided ? dispatch_pack_fp8_kernel<KMAX, true> : dispatch_pack_fp8_kernel<KMAX, false>;
-  const size_t smem = pack_fp8_smem_bytes(stages, p.H);
+  auto* kern = p.queue ? dispatch_pack_fp8_queue_kernel<KMAX>
+               : strided ? dispatch_pack_fp8_kernel<KMAX, true>
+                         : dispatch_pack_fp8_kernel<KMAX, false>;
+  const size_t smem = pack_fp8_smem_bytes(stages, p.H, p.queue != nullptr);
   cudaError_t err = set_kernel_limits(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   // A persistent grid larger than what can be resident runs a second wave:
@@ -208,8 +338,8 @@ cudaError_t launch_fp8_k(const PackFp8Params& p, int sms, int per_sm, int stages
 
 }  // namespace
 
-size_t pack_fp8_smem_bytes(int stages, int H) {
-  return kFp8BarBytes + static_cast<size_t>(stages) * H * 2;
+size_t pack_fp8_smem_bytes(int stages, int H, bool queue) {
+  return (queue ? kFp8QueueHeaderBytes : kFp8BarBytes) + static_cast<size_t>(stages) * H * 2;
 }
 
 int pack_fp8_max_stages() { return kMaxFp8Stages; }

@@ -855,6 +855,19 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
     const int want = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : (few_dest ? 8 : 3);
     if (per_sm > want) per_sm = want;
     if (per_sm < 1) per_sm = 1;
+    // Token queue (MOE_OPT_PACK_SCHEDULE; strided order only): automatic when a
+    // CTA has more than three prologues (`stages` tokens) of work; the static
+    // split otherwise, or if the queue's larger shared-memory header would not
+    // fit.  Measured on GB300 (A/B, one box): Kimi-sized fp8 layer 543.1 ->
+    // 520.9 us with the queue; DeepSeek-sized (9 tokens per CTA, 5 stages)
+    // 139.1 -> 140.4 and Mixtral-sized 34.2 -> 35.0, so those stay static.
+    if (ctx->fp8_order == 1 && ctx->pack_schedule != 0 &&
+        moe::pack_fp8_smem_bytes(stages, c.hidden, true) <= static_cast<size_t>(ctx->max_smem_optin)) {
+      int64_t grid = static_cast<int64_t>(grid_sms(ctx)) * per_sm;
+      if (grid > c.num_tokens) grid = c.num_tokens;
+      if (ctx->pack_schedule == 1 || static_cast<int64_t>(c.num_tokens) > 3 * static_cast<int64_t>(stages) * grid)
+        fp.queue = ctx->queue;
+    }
     const bool timed = ctx->kernel_events != 0;
     if (timed && cudaEventRecord(ctx->ev[0], s) != cudaSuccess) return MOE_ECUDA;
     if (moe::launch_dispatch_pack_fp8(fp, grid_sms(ctx), per_sm, stages, ctx->pdl != 0, ctx->fp8_order == 1, s) !=

@@ -128,12 +128,14 @@ struct PackFp8Params {
   int32_t* error_word;
   int32_t T, K, H;          // H % 128 == 0
   int64_t dst_rows;         // rows of expert_xq / expert_scales (checked builds)
+  unsigned long long* queue;  // [1] token queue, 0 at launch (set by routing); null: static split
 };
-size_t pack_fp8_smem_bytes(int stages, int H);
+size_t pack_fp8_smem_bytes(int stages, int H, bool queue = false);
 int pack_fp8_max_stages();
 // Persistent grid of up to sms x per_sm CTAs (fewer if fewer can be resident
-// or T is smaller); strided: CTA b packs tokens b, b+grid, ...; else one
-// contiguous token range.
+// or T is smaller); with p.queue: each CTA's first `stages` tokens b, b+grid,
+// ... then tokens claimed from the queue; else strided: CTA b packs tokens b,
+// b+grid, ...; else one contiguous token range.
 cudaError_t launch_dispatch_pack_fp8(const PackFp8Params& p, int sms, int per_sm, int stages, bool pdl, bool strided,
                                      cudaStream_t stream);
 

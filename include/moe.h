@@ -353,7 +353,9 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
 #define MOE_OPT_KERNEL_EVENTS 19
 /*   MOE_OPT_PACK_SCHEDULE       bulk pack of moe_dispatch_send and of the
  *                               first stage of the staged and quantised
- *                               dispatches: 0 = static (CTA b copies units b,
+ *                               dispatches, and (with MOE_OPT_FP8_ORDER 1,
+ *                               tokens as units) the pack of
+ *                               moe_dispatch_send_fp8: 0 = static (CTA b copies units b,
  *                               b+G, b+2G, ... of the G CTAs); 1 = unit queue
  *                               (each CTA takes its first `stages` units
  *                               statically, then claims units in increasing
@@ -361,7 +363,8 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               routing kernel resets, so faster CTAs take
  *                               more); -1 = automatic (default: the queue when
  *                               a CTA has more than 1.5x its first `stages`
- *                               units).  Results are identical. */
+ *                               units, 3x for the fp8 pack).  Results are
+ *                               identical. */
 #define MOE_OPT_PACK_SCHEDULE 20
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 

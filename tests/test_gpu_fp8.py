@@ -67,11 +67,12 @@ def check(res, oracle_mod, w, li):
         assert np.array_equal(res["out"], oracle_mod.combine(li.y, li.topk_w, d.slot_row))
 
 
+@pytest.mark.parametrize("pack_schedule", [-1, 0, 1])
 @pytest.mark.parametrize("name", [w.name for w in gen.WORKLOADS])
-def test_fp8_named_workloads(moe, oracle_mod, name):
+def test_fp8_named_workloads(moe, oracle_mod, name, pack_schedule):
     w = gen.BY_NAME[name]
     li = gen.make_inputs(w)
-    check(run_fp8(moe, w, li), oracle_mod, w, li)
+    check(run_fp8(moe, w, li, pack_schedule=pack_schedule), oracle_mod, w, li)
 
 
 FP8_EDGE = [
@@ -82,9 +83,10 @@ FP8_EDGE = [
 ]
 
 
+@pytest.mark.parametrize("pack_schedule", [0, 1])
 @pytest.mark.parametrize("route_variant", [0, 1, 2])
 @pytest.mark.parametrize("shape", FP8_EDGE, ids=["x".join(map(str, s)) for s in FP8_EDGE])
-def test_fp8_edge_shapes(moe, oracle_mod, shape, route_variant):
+def test_fp8_edge_shapes(moe, oracle_mod, shape, route_variant, pack_schedule):
     T, H, K, E, N = shape
     w = gen.custom("fp8edge", T=T, H=H, K=K, E=E, N=N, seed_index=17)
     li = gen.make_inputs(w)
@@ -92,7 +94,7 @@ def test_fp8_edge_shapes(moe, oracle_mod, shape, route_variant):
     xf = gen.bf16_bits_to_f32(li.x) * np.exp(np.random.default_rng(3).uniform(-8, 8, (T, 1))).astype(np.float32)
     xf[0, :128] = 0.0
     li = gen.LayerInputs(w, gen.to_bf16_bits(xf), li.topk_idx, li.topk_w, li.y)
-    check(run_fp8(moe, w, li, route_variant=route_variant), oracle_mod, w, li)
+    check(run_fp8(moe, w, li, route_variant=route_variant, pack_schedule=pack_schedule), oracle_mod, w, li)
 
 
 @pytest.mark.parametrize("name", ["tiny", "mixtral", "deepseek"])
@@ -110,12 +112,13 @@ def test_fp8_contiguous_edge_shapes(moe, oracle_mod, shape):
     check(run_fp8(moe, w, li, fp8_order=0), oracle_mod, w, li)
 
 
-def test_fp8_routing_error_writes_nothing(moe):
+@pytest.mark.parametrize("pack_schedule", [0, 1])
+def test_fp8_routing_error_writes_nothing(moe, pack_schedule):
     w = gen.custom("fp8bad", T=64, H=256, K=2, E=8, N=2, seed_index=19)
     li = gen.make_inputs(w)
     idx = li.topk_idx.copy()
     idx[5, 1] = 99
-    res = run_fp8(moe, w, gen.LayerInputs(w, li.x, idx, li.topk_w, li.y))
+    res = run_fp8(moe, w, gen.LayerInputs(w, li.x, idx, li.topk_w, li.y), pack_schedule=pack_schedule)
     assert res["status"] == moe.MOE_EROUTE
     assert res["guards"]
     assert np.all(res["xq"] == CANARY8) and np.all(res["xs"] == CANARYF)
