@@ -531,7 +531,8 @@ def run_gpu(args):
                                    else "two-stage: per-peer send rows, then receive shuffle",
                        "pack": f"bulk (TMA), {layer.get_option(moe.MOE_OPT_PACK_STAGES) or 'auto'} stages, "
                                f"prefetch={layer.get_option(moe.MOE_OPT_PACK_PREFETCH)}, "
-                               f"hints={layer.get_option(moe.MOE_OPT_CACHE_HINTS)}, PDL",
+                               f"hints={layer.get_option(moe.MOE_OPT_CACHE_HINTS)}, PDL, "
+                               f"schedule={ {-1: 'auto', 0: 'static', 1: 'queue'}[layer.get_option(moe.MOE_OPT_PACK_SCHEDULE)]}",
                        "combine": ("two-level: sending-side partial sums, "
                                    f"{partial_rows} partial rows" if args.combine == "two_level"
                                    else "bulk (TMA gather)" if layer.get_option(moe.MOE_OPT_COMBINE_VARIANT) == 0

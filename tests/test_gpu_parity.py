@@ -397,9 +397,13 @@ def test_call_order_and_argument_checks(moe):
     layer.combine_recv(wt, out)
     assert layer.get_error() == moe.MOE_OK
     for opt, val in [(moe.MOE_OPT_PACK_STAGES, 1), (moe.MOE_OPT_PACK_VARIANT, 5),
-                     (moe.MOE_OPT_PACK_PIECE_BYTES, 24), (99, 0)]:
+                     (moe.MOE_OPT_PACK_PIECE_BYTES, 24), (moe.MOE_OPT_PACK_SCHEDULE, 2),
+                     (moe.MOE_OPT_PACK_SCHEDULE, -2), (99, 0)]:
         with pytest.raises(moe.MoEError):
             layer.set_option(opt, val)
+    assert layer.get_option(moe.MOE_OPT_PACK_SCHEDULE) == -1  # automatic by default
+    layer.set_option(moe.MOE_OPT_PACK_SCHEDULE, 1)
+    assert layer.get_option(moe.MOE_OPT_PACK_SCHEDULE) == 1
 
 
 def test_repeat_runs_are_byte_identical(moe):
