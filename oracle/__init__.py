@@ -28,6 +28,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.cc")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_SELFTEST_SRC = os.path.join(_HERE, "selftest.cc")
+SELFTEST = os.path.join(_HERE, "oracle_selftest")  # the self-test program, built by build()
 
 OK, EINVAL, EROUTE, EBOUND = 0, 1, 3, 5
 
@@ -43,6 +45,12 @@ def build(force: bool = False) -> str:
                "-fPIC", "-shared", "-o", tmp, _SRC]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_SELFTEST_SRC))
+    if force or not os.path.exists(SELFTEST) or os.path.getmtime(SELFTEST) < newest:
+        tmp = SELFTEST + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SELFTEST_SRC, _SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, SELFTEST)
     return _LIB
 
 
