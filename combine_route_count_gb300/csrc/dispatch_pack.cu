@@ -11,6 +11,8 @@
 //
 // Each token row is read from HBM once and written K times.  Work is split
 // into units (token t, piece j of the row); CTA b takes units b, b+G, b+2G...
+// (static split), or its first `stages` of those and then units claimed from
+// a queue in the workspace (dispatch_pack_bulk_queue, below).
 //
 // Bulk variant (default): one warp per CTA drives the TMA engine.  Lane 0
 // loads a piece into a shared-memory stage with cp.async.bulk (completion on
