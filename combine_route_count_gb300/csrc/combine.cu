@@ -333,14 +333,213 @@ __global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_kernel(Combin
   }
 }
 
+// Token queue.  The static orders give every CTA the same number of units,
+// but inside a layer the CTAs do not progress at the same rate (the write-back
+// of the previous kernel's dirty lines and DRAM contention fall unevenly), so
+// the last CTAs finish well after the median one.  Here CTA b takes token b,
+// then claims tokens G, G+1, ... from a counter that the routing kernel sets
+// to 0, and copies all P pieces of each claimed token one after another (as
+// in the static orders, whose row locality this keeps).  The producer
+// publishes each stage's unit (t*P + j) and its K weights in shared memory
+// before the stage's full barrier completes, loads the next unit's rows and
+// weights while the current one is issued, and keeps two claims in flight.
+// Unit -1 ends a CTA's sequence.
+constexpr int kBulkQueueHeaderBytes = 1024;  // full[8], empty[8], skip[8], stage_unit[8], stage_w[8][16]
+
+template <int KMAX>
+__global__ void __launch_bounds__(kBulkMaxThreads, 2) combine_bulk_queue_kernel(CombineParams p, BulkCombineShape sh) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kMaxBulkStages;
+  int32_t* skip = reinterpret_cast<int32_t*>(empty + kMaxBulkStages);
+  int64_t* stage_unit = reinterpret_cast<int64_t*>(skip + kMaxBulkStages);
+  float* stage_w = reinterpret_cast<float*>(stage_unit + kMaxBulkStages);  // [kMaxBulkStages][MOE_MAX_TOP_K]
+  uint8_t* stage_buf = smem + kBulkQueueHeaderBytes;
+  const int S = sh.stages, P = sh.pieces, PB = sh.piece_bytes;
+  const int K = p.K;
+  const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
+  const int64_t stage_bytes = static_cast<int64_t>(K) * PB;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int consumer_warps = (blockDim.x >> 5) - 1;
+  const int64_t G = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], consumer_warps);
+    }
+    ptx::mbar_fence_init();
+  }
+  __syncthreads();
+  ptx::wait_prerequisites();  // y and slot_row come from earlier kernels; routing reset the queue
+
+  auto piece_len = [&](int j) -> uint32_t {
+    const int64_t left = row_bytes - static_cast<int64_t>(j) * PB;
+    return static_cast<uint32_t>(left < PB ? left : PB);
+  };
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    const uint64_t pol = sh.hints ? ptx::policy_evict_first() : 0;
+    // Lane 0: this CTA's next unit (called in order); -1 = none.  Token b
+    // first, then tokens G, G+1, ... claimed whole: all P pieces of a token
+    // go to the CTA that claimed it, one after another.
+    bool claiming = static_cast<int64_t>(p.T) > G;
+    unsigned long long q0 = 0, q1 = 0;
+    if (lane == 0 && claiming) {
+      q0 = atomicAdd(p.queue, 1ull);
+      q1 = atomicAdd(p.queue, 1ull);
+    }
+    bool first = true;
+    int64_t tok = -1;
+    int jj = P;
+    auto unit_of = [&](int64_t) -> int64_t {
+      if (jj >= P) {
+        if (first) {
+          first = false;
+          tok = blockIdx.x < p.T ? static_cast<int64_t>(blockIdx.x) : -1;
+        } else if (!claiming) {
+          tok = -1;
+        } else {
+          const int64_t c = G + static_cast<int64_t>(q0);
+          if (c >= p.T) {
+            claiming = false;
+            tok = -1;
+          } else {
+            tok = c;
+            q0 = q1;
+            q1 = atomicAdd(p.queue, 1ull);
+          }
+        }
+        jj = 0;
+        if (tok < 0) return -1;
+      }
+      return tok * P + jj++;
+    };
+    // Rows and weight of unit u for lane k < K.
+    auto fetch = [&](int64_t u, int& row, float& wk) {
+      row = -1;
+      wk = 0.0f;
+      if (u >= 0 && lane < K) {
+        const int64_t t = u / P;
+        row = p.slot_row[t * K + lane];
+        wk = __ldg(p.w + t * K + lane);
+      }
+    };
+    int64_t u_cur = 0;
+    if (lane == 0) u_cur = unit_of(0);
+    u_cur = __shfl_sync(0xffffffffu, u_cur, 0);
+    int row, nrow;
+    float wk, nw;
+    fetch(u_cur, row, wk);
+    bool ok = true;
+    for (int64_t i = 0;; ++i) {
+      const int s = static_cast<int>(i % S);
+      int64_t u_nxt = 0;
+      if (lane == 0) u_nxt = u_cur >= 0 ? unit_of(i + 1) : -1;
+      u_nxt = __shfl_sync(0xffffffffu, u_nxt, 0);
+      fetch(u_nxt, nrow, nw);
+      if (i >= S) {
+        const bool freed = wait_parity(&empty[s], static_cast<uint32_t>(((i / S) - 1) & 1));
+        if (!__all_sync(0xffffffffu, freed)) {
+          ok = false;
+          break;
+        }
+      }
+      if (u_cur < 0) {
+        if (lane == 0) {
+          stage_unit[s] = -1;
+          mbar_arrive(&full[s]);  // the end of this CTA's sequence
+        }
+        break;
+      }
+      const int j = static_cast<int>(u_cur % P);
+      const bool out_of_range = kChecked && lane < K && row >= p.y_rows;
+      if (out_of_range) atomicCAS(p.error_word, MOE_OK, MOE_ECORRUPT);
+      const bool bad = __any_sync(0xffffffffu, lane < K && (row < 0 || out_of_range));
+      const uint32_t bytes = piece_len(j);
+      if (lane < K) stage_w[s * MOE_MAX_TOP_K + lane] = wk;
+      if (lane == 0) {
+        stage_unit[s] = u_cur;
+        skip[s] = bad ? 1 : 0;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (bad)
+          mbar_arrive(&full[s]);  // nothing to load: release the consumers, who skip the unit
+        else
+          ptx::mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(K) * bytes);
+      }
+      __syncwarp();
+      if (!bad && lane < K) {
+        uint8_t* dst = stage_buf + s * stage_bytes + static_cast<int64_t>(lane) * PB;
+        const uint8_t* src = p.y + static_cast<int64_t>(row) * row_bytes + static_cast<int64_t>(j) * PB;
+        if (sh.hints & kHintCombineLoads)
+          ptx::bulk_g2s_hint(dst, src, bytes, &full[s], pol);
+        else
+          ptx::bulk_g2s(dst, src, bytes, &full[s]);
+      }
+      u_cur = u_nxt;
+      row = nrow;
+      wk = nw;
+    }
+    if (!ok && lane == 0) atomicCAS(p.error_word, MOE_OK, MOE_ETIMEDOUT);
+  } else {
+    // ---------------- consumers ----------------
+    const int c = threadIdx.x - 32;  // 16-byte column chunk within the piece
+    for (int64_t i = 0;; ++i) {
+      const int s = static_cast<int>(i % S);
+      const bool arrived = wait_parity(&full[s], static_cast<uint32_t>((i / S) & 1));
+      if (!__all_sync(0xffffffffu, arrived)) {
+        if (lane == 0) atomicCAS(p.error_word, MOE_OK, MOE_ETIMEDOUT);
+        break;
+      }
+      const int64_t u = stage_unit[s];
+      if (u < 0) break;
+      const int64_t t = u / P;
+      const int j = static_cast<int>(u - t * P);
+      const uint32_t bytes = piece_len(j);
+      if (!skip[s] && static_cast<uint32_t>(c) * 16 < bytes) {
+        const uint8_t* src = stage_buf + s * stage_bytes + static_cast<int64_t>(c) * 16;
+        uint4 v[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+          if (k < K) v[k] = lds128(src + static_cast<int64_t>(k) * PB);
+        float a[8];
+#pragma unroll
+        for (int q2 = 0; q2 < 8; ++q2) a[q2] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+          if (k < K) {
+            const float w = stage_w[s * MOE_MAX_TOP_K + k];
+            fma_word(v[k].x, w, a[0], a[1]);
+            fma_word(v[k].y, w, a[2], a[3]);
+            fma_word(v[k].z, w, a[4], a[5]);
+            fma_word(v[k].w, w, a[6], a[7]);
+          }
+        }
+        uint4 o;
+        o.x = pack_bf16x2(a[0], a[1]);
+        o.y = pack_bf16x2(a[2], a[3]);
+        o.z = pack_bf16x2(a[4], a[5]);
+        o.w = pack_bf16x2(a[6], a[7]);
+        ptx::st_v4(p.out + t * row_bytes + static_cast<int64_t>(j) * PB + static_cast<int64_t>(c) * 16, o);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+}
+
 template <int KMAX>
 cudaError_t launch_bulk_k(const CombineParams& p, const CombineLaunch& l, cudaStream_t stream) {
   const BulkCombineShape& sh = l.shape;
   const size_t smem = combine_bulk_smem_bytes(sh, p.K);
-  auto* kern = sh.strided ? (sh.drop_unit >= 0 ? combine_bulk_kernel<KMAX, true, true>
-                                              : combine_bulk_kernel<KMAX, false, true>)
-                          : (sh.drop_unit >= 0 ? combine_bulk_kernel<KMAX, true, false>
-                                              : combine_bulk_kernel<KMAX, false, false>);
+  auto* kern = sh.queue && p.queue ? combine_bulk_queue_kernel<KMAX>
+               : sh.strided ? (sh.drop_unit >= 0 ? combine_bulk_kernel<KMAX, true, true>
+                                                 : combine_bulk_kernel<KMAX, false, true>)
+                            : (sh.drop_unit >= 0 ? combine_bulk_kernel<KMAX, true, false>
+                                                 : combine_bulk_kernel<KMAX, false, false>);
   cudaError_t err = set_kernel_limits(reinterpret_cast<const void*>(kern), smem);
   if (err != cudaSuccess) return err;
   const int threads = 32 + (sh.piece_bytes / 16 + 31) / 32 * 32;
@@ -361,7 +560,7 @@ cudaError_t launch_k(const CombineParams& p, bool pdl, cudaStream_t stream) {
 }  // namespace
 
 size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K) {
-  return kBulkBarBytes + static_cast<size_t>(sh.stages) * K * sh.piece_bytes;
+  return (sh.queue ? kBulkQueueHeaderBytes : kBulkBarBytes) + static_cast<size_t>(sh.stages) * K * sh.piece_bytes;
 }
 
 BulkCombineShape combine_bulk_shape(int H, int K, int stages, int piece_bytes, int max_smem, int auto_piece_max) {

@@ -125,8 +125,8 @@ WorkspaceLayout layout_of(const moe_config& c) {
   o += align_up(sizeof(float) * pairs);
   l.plan_mask = o;
   o += align_up(sizeof(int32_t) * static_cast<size_t>(c.num_tokens));
-  l.queue = o;  // the bulk pack's unit queue (set to 0 by the routing kernel of every dispatch)
-  o += align_up(sizeof(unsigned long long));
+  l.queue = o;  // the pack's and the combine's unit queues (set to 0 by the routing of every dispatch)
+  o += align_up(2 * sizeof(unsigned long long));
   l.total = o;
   return l;
 }
@@ -178,6 +178,7 @@ struct moe_ctx {
   int cache_hints;       // MOE_OPT_CACHE_HINTS bit flags
   int pack_depth;        // MOE_OPT_PACK_STORE_DEPTH (0 = default)
   int pack_schedule;     // MOE_OPT_PACK_SCHEDULE (-1 = automatic)
+  int combine_schedule;  // MOE_OPT_COMBINE_SCHEDULE (-1 = automatic)
   int pdl;
   int route_variant;  // MOE_OPT_ROUTE_VARIANT
   int combine_variant;      // MOE_OPT_COMBINE_VARIANT
@@ -266,6 +267,7 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   c->plan_mask = reinterpret_cast<int32_t*>(c->ws + l.plan_mask);
   c->queue = reinterpret_cast<unsigned long long*>(c->ws + l.queue);
   c->pack_schedule = -1;
+  c->combine_schedule = -1;
   c->pack_variant = moe::kPackBulk;
   c->pack_stages = 0;  // automatic: about 200 KiB of stages per SM
   c->pack_prefetch = 2;
@@ -372,6 +374,10 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       if (value < -1 || value > 1) return MOE_EINVAL;
       ctx->pack_schedule = static_cast<int>(value);
       return MOE_OK;
+    case MOE_OPT_COMBINE_SCHEDULE:
+      if (value < -1 || value > 1) return MOE_EINVAL;
+      ctx->combine_schedule = static_cast<int>(value);
+      return MOE_OK;
     case MOE_OPT_COMBINE_VARIANT:
       if (value != -1 && value != moe::kCombineBulk && value != moe::kCombineVector) return MOE_EINVAL;
       ctx->combine_variant = static_cast<int>(value);
@@ -456,6 +462,9 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
       return MOE_OK;
     case MOE_OPT_PACK_SCHEDULE:
       *value = ctx->pack_schedule;
+      return MOE_OK;
+    case MOE_OPT_COMBINE_SCHEDULE:
+      *value = ctx->combine_schedule;
       return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
       *value = ctx->route_variant != 0 ? ctx->route_variant : (ctx->cluster_ctas > 0 ? 3 : 2);
@@ -944,6 +953,19 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
                                          ctx->max_smem_optin, strided ? 4096 : 2048);
       cl.shape.hints = ctx->cache_hints;
       cl.shape.drop_unit = ctx->test_drop_unit;
+      // Token queue (MOE_OPT_COMBINE_SCHEDULE; default on, not with the
+      // failure-injection hook).  Measured on GB300 (A/B, one box) against the
+      // strided static order: DeepSeek-sized layer 162.7 -> 160.4 us,
+      // Kimi-sized 659.2 -> 645.0, worst case 325.0 -> 318.1.  Claiming single
+      // (token, piece) units instead was slower than the static order
+      // (DeepSeek 164.0 -> 168.3, Kimi 661 -> 702): pieces of one token read
+      // by different CTAs at once lose the row locality of one CTA streaming
+      // a token's K rows piece after piece.
+      cl.shape.queue = ctx->combine_schedule != 0 && ctx->test_drop_unit < 0 ? 1 : 0;
+      if (cl.shape.queue &&
+          moe::combine_bulk_smem_bytes(cl.shape, c.top_k) > static_cast<size_t>(ctx->max_smem_optin))
+        cl.shape.queue = 0;
+      if (cl.shape.queue) cp.queue = ctx->queue + 1;
       const size_t smem = moe::combine_bulk_smem_bytes(cl.shape, c.top_k);
       if (smem > static_cast<size_t>(ctx->max_smem_optin)) return MOE_EINVAL;
       const int fit = static_cast<int>((228 * 1024) / (smem + 1024));

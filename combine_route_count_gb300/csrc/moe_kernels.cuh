@@ -32,7 +32,7 @@ struct RouteCountParams {
   int32_t* slot_row;        // [T*K]
   int32_t* row_src;         // [T*K]
   int32_t* error_word;      // [1]
-  unsigned long long* queue;  // [1] the bulk pack's unit queue: set to 0 here (may be null)
+  unsigned long long* queue;  // [2] the pack's and the combine's unit queues: set to 0 here (may be null)
 };
 constexpr int kRouteThreads = 1024;
 // Dynamic shared memory the kernel needs for E experts.
@@ -54,7 +54,7 @@ struct RouteSplitParams {
   int32_t* slot_row;        // [T*K]
   int32_t* row_src;         // [T*K]
   int32_t* error_word;      // [1]
-  unsigned long long* queue;  // [1] the bulk pack's unit queue: set to 0 here (may be null)
+  unsigned long long* queue;  // [2] the pack's and the combine's unit queues: set to 0 here (may be null)
   int32_t* hist;            // [blocks*E] per-chunk expert histograms
   int32_t* block_err;       // [blocks]   per-chunk routing error flags
 };
@@ -79,7 +79,7 @@ struct RouteClusterParams {
   int32_t* slot_row;        // [T*K]
   int32_t* row_src;         // [T*K]
   int32_t* error_word;      // [1]
-  unsigned long long* queue;  // [1] the bulk pack's unit queue: set to 0 here (may be null)
+  unsigned long long* queue;  // [2] the pack's and the combine's unit queues: set to 0 here (may be null)
 };
 size_t route_cluster_smem_bytes(int E, int warps, int staged_pairs);
 // Fills chunk/warps/staged/dsmem_group of p for a cluster of `cluster` CTAs.
@@ -148,6 +148,7 @@ struct CombineParams {
   int32_t* error_word;      // [1] bounded waits report MOE_ETIMEDOUT here
   int32_t T, K, H;
   int64_t y_rows;           // rows of y (checked builds verify slot_row against it)
+  unsigned long long* queue;  // [1] unit queue of the bulk combine, 0 at launch (set by routing)
 };
 enum CombineVariant { kCombineBulk = 0, kCombineVector = 1 };
 struct BulkCombineShape {
@@ -157,6 +158,7 @@ struct BulkCombineShape {
   int hints;           // CacheHints
   int64_t drop_unit;   // failure-injection hook: unit the producer never posts (-1: none)
   int strided;         // 1: a CTA takes tokens b, b+G, ...; 0: a contiguous unit range
+  int queue;           // 1: units claimed from CombineParams::queue after the first `stages`
 };
 struct CombineLaunch {
   int variant;             // CombineVariant

@@ -194,9 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1) route_cluster_kernel(RouteCluster
   // then let the pack kernel start fetching token rows.
   ptx::wait_prerequisites();
   ptx::launch_dependents();
-  // The pack's unit queue restarts at 0 for this layer; the pack claims from
-  // it only after this grid has completed.
-  if (p.queue && rank == 0 && tid == 0) *p.queue = 0ull;
+  // The pack's and the combine's unit queues restart at 0 for this layer;
+  // units are claimed from them only after this grid has completed.
+  if (p.queue && rank == 0 && tid == 0) {
+    p.queue[0] = 0ull;  // the pack's units
+    p.queue[1] = 0ull;  // the combine's units
+  }
 
   // First sub-chunk's indices are requested before the shared-memory set-up.
   int e[KMAX], r[KMAX];

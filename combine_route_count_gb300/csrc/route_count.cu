@@ -138,10 +138,14 @@ __global__ void __launch_bounds__(kThreads, 1) route_count_kernel(RouteCountPara
   // The pack kernel may start loading token rows now: they do not depend on
   // anything this kernel writes.
   ptx::launch_dependents();
-  // The pack's unit queue restarts at 0 for this layer (the pack claims from
-  // it only after this grid has completed).  Launched without programmatic
-  // serialisation, this kernel starts after every earlier kernel has ended.
-  if (p.queue && tid == 0) *p.queue = 0ull;
+  // The pack's and the combine's unit queues restart at 0 for this layer
+  // (units are claimed from them only after this grid has completed).
+  // Launched without programmatic serialisation, this kernel starts after
+  // every earlier kernel has ended.
+  if (p.queue && tid == 0) {
+    p.queue[0] = 0ull;  // the pack's units
+    p.queue[1] = 0ull;  // the combine's units
+  }
 
   for (int i = tid; i < E; i += kThreads) sm.cnt[i] = 0;
   __syncthreads();

@@ -94,9 +94,13 @@ __global__ void __launch_bounds__(kThreads) route_local_kernel(RouteSplitParams 
   const int Tr = T / N;
 
   ptx::launch_dependents();
-  // The pack's unit queue restarts at 0 (this kernel is launched without
-  // programmatic serialisation: every earlier kernel has ended).
-  if (p.queue && c == 0 && tid == 0) *p.queue = 0ull;
+  // The pack's and the combine's unit queues restart at 0 (this kernel is
+  // launched without programmatic serialisation: every earlier kernel has
+  // ended).
+  if (p.queue && c == 0 && tid == 0) {
+    p.queue[0] = 0ull;  // the pack's units
+    p.queue[1] = 0ull;  // the combine's units
+  }
 
   for (int i = tid; i < E; i += kThreads) carry[i] = 0;
   bool bad = false;

@@ -36,6 +36,7 @@ MOE_OPT_COMBINE_ORDER = 17
 MOE_OPT_FP8_ORDER = 18
 MOE_OPT_KERNEL_EVENTS = 19
 MOE_OPT_PACK_SCHEDULE = 20
+MOE_OPT_COMBINE_SCHEDULE = 21
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.
@@ -341,7 +342,7 @@ class MoELayer:
                  "cache_hints": MOE_OPT_CACHE_HINTS, "pack_store_depth": MOE_OPT_PACK_STORE_DEPTH,
                  "max_sms": MOE_OPT_MAX_SMS, "combine_order": MOE_OPT_COMBINE_ORDER,
                  "fp8_order": MOE_OPT_FP8_ORDER, "kernel_events": MOE_OPT_KERNEL_EVENTS,
-                 "pack_schedule": MOE_OPT_PACK_SCHEDULE}
+                 "pack_schedule": MOE_OPT_PACK_SCHEDULE, "combine_schedule": MOE_OPT_COMBINE_SCHEDULE}
         for k, v in options.items():
             moe_ctx_set_option(self.ctx, names[k], int(v))
 

@@ -366,6 +366,15 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
  *                               units, 3x for the fp8 pack).  Results are
  *                               identical. */
 #define MOE_OPT_PACK_SCHEDULE 20
+/*   MOE_OPT_COMBINE_SCHEDULE    bulk combine of moe_combine_recv: 0 = the
+ *                               static order of MOE_OPT_COMBINE_ORDER; 1 =
+ *                               token queue (CTA b combines token b, then
+ *                               claims tokens in increasing order from a
+ *                               counter in the workspace that the routing
+ *                               kernel resets, all pieces of a claimed token
+ *                               in turn); -1 = automatic (default: the queue).
+ *                               Results are identical. */
+#define MOE_OPT_COMBINE_SCHEDULE 21
 int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value);
 
 /* Durations, in milliseconds, of the pack kernel of the context's last

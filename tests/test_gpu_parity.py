@@ -175,6 +175,13 @@ PACK_OPTIONS = [
     dict(pack_schedule=1, pack_prefetch=0, cache_hints=0, pdl=0),
     dict(pack_schedule=1, route_variant=1),
     dict(pack_schedule=1, route_variant=2),
+    dict(combine_variant=0, combine_schedule=0),
+    dict(combine_variant=0, combine_schedule=1),
+    dict(combine_variant=0, combine_schedule=1, combine_stages=2, combine_piece_bytes=1024),
+    dict(combine_variant=0, combine_schedule=1, combine_stages=8, combine_piece_bytes=2048 + 16,
+         combine_ctas_per_sm=1),
+    dict(combine_variant=0, combine_schedule=1, pdl=0, route_variant=1),
+    dict(combine_variant=0, combine_schedule=1, pack_schedule=1, route_variant=2),
 ]
 
 
@@ -245,12 +252,24 @@ def test_edge_shapes_pack_queue(moe, oracle_mod, shape):
     assert_parity(res, d, out_ref, w, extra_rows=2)
 
 
+@pytest.mark.parametrize("shape", EDGE, ids=["x".join(map(str, s[:5])) for s in EDGE])
+def test_edge_shapes_combine_queue(moe, oracle_mod, shape):
+    """The bulk combine with its unit queue forced on, at every edge shape."""
+    T, H, K, E, N, router = shape
+    w = gen.custom("edge", T=T, H=H, K=K, E=E, N=N, router=router, seed_index=19)
+    li = gen.make_inputs(w)
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    res = run_gpu(moe, w, li, extra_rows=2, combine_variant=0, combine_schedule=1)
+    assert_parity(res, d, out_ref, w, extra_rows=2)
+
+
 def test_pack_queue_is_reset_every_layer(moe, oracle_mod):
-    """Layers with different routings on one context, the queue forced on:
-    each layer's routing resets the queue (a stale count would leave units
-    uncopied), also across a routing error and with each routing variant."""
+    """Layers with different routings on one context, the pack's and the
+    combine's queues forced on: each layer's routing resets both (a stale
+    count would leave units undone), also across a routing error and with
+    each routing variant."""
     T, H, K, E, N = 2048, 1024, 8, 64, 8
-    layer = moe.MoELayer(T, H, K, E, N, pack_schedule=1)
+    layer = moe.MoELayer(T, H, K, E, N, pack_schedule=1, combine_variant=0, combine_schedule=1)
     ex = torch.empty((T * K, H), dtype=torch.int16, device="cuda")
     out = torch.empty((T, H), dtype=torch.int16, device="cuda")
     for n, route in enumerate([0, 0, 1, 2, 3, 0]):
@@ -402,6 +421,9 @@ def test_call_order_and_argument_checks(moe):
         with pytest.raises(moe.MoEError):
             layer.set_option(opt, val)
     assert layer.get_option(moe.MOE_OPT_PACK_SCHEDULE) == -1  # automatic by default
+    assert layer.get_option(moe.MOE_OPT_COMBINE_SCHEDULE) == -1
+    with pytest.raises(moe.MoEError):
+        layer.set_option(moe.MOE_OPT_COMBINE_SCHEDULE, 3)
     layer.set_option(moe.MOE_OPT_PACK_SCHEDULE, 1)
     assert layer.get_option(moe.MOE_OPT_PACK_SCHEDULE) == 1
 
