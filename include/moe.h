@@ -93,8 +93,9 @@ int moe_validate_config(const moe_config* cfg);
 /* Device workspace (bytes, a multiple of 256) that one context needs: counts,
  * offsets, slot_row, row_src, the error word, the send tables of
  * moe_dispatch_send_staged, the plan of moe_combine_recv_two_level and the
- * pack's unit queue.  Allocate it 256-byte aligned; its contents need no
- * initialisation (every dispatch writes what it later reads). */
+ * pack's and the combine's work-queue counters.  Allocate it 256-byte
+ * aligned; its contents need no initialisation (every dispatch writes what it
+ * later reads). */
 int moe_workspace_bytes(const moe_config* cfg, size_t* bytes);
 
 /* The receive bound of "Enabling trillion-parameter models on AWS EFA"
