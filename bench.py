@@ -535,7 +535,9 @@ def run_gpu(args):
                                f"schedule={ {-1: 'auto', 0: 'static', 1: 'queue'}[layer.get_option(moe.MOE_OPT_PACK_SCHEDULE)]}",
                        "combine": ("two-level: sending-side partial sums, "
                                    f"{partial_rows} partial rows" if args.combine == "two_level"
-                                   else "bulk (TMA gather)" if layer.get_option(moe.MOE_OPT_COMBINE_VARIANT) == 0
+                                   else "bulk (TMA gather), " + ("static order" if layer.get_option(
+                                       moe.MOE_OPT_COMBINE_SCHEDULE) == 0 else "token queue")
+                                   if layer.get_option(moe.MOE_OPT_COMBINE_VARIANT) == 0
                                    else "vector"),
                        "routing": {1: "route_count (1 block)", 2: "route_local+route_finalize",
                                    3: f"route_cluster ({layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS)} CTAs)"}[
