@@ -29,11 +29,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.cc")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _SELFTEST_SRC = os.path.join(_HERE, "selftest.cc")
+_PAR_SRC = os.path.join(_HERE, "moe_oracle_par.cc")
+_PAR_LIB = os.path.join(_HERE, "liboracle_par.so")  # the same loops over every host core (OpenMP)
 SELFTEST = os.path.join(_HERE, "oracle_selftest")  # the self-test program, built by build()
 
 OK, EINVAL, EROUTE, EBOUND = 0, 1, 3, 5
 
 _lib: Optional[ctypes.CDLL] = None
+_par: Optional[ctypes.CDLL] = None
 
 
 def build(force: bool = False) -> str:
@@ -51,6 +54,13 @@ def build(force: bool = False) -> str:
         cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SELFTEST_SRC, _SRC]
         subprocess.run(cmd, check=True)
         os.replace(tmp, SELFTEST)
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_PAR_SRC))
+    if force or not os.path.exists(_PAR_LIB) or os.path.getmtime(_PAR_LIB) < newest:
+        tmp = _PAR_LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+               "-fPIC", "-shared", "-o", tmp, _PAR_SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _PAR_LIB)
     return _LIB
 
 
@@ -84,6 +94,22 @@ def _load() -> ctypes.CDLL:
         lib.oracle_e4m3_to_double.restype = ctypes.c_double
         _lib = lib
     return _lib
+
+
+def _load_par() -> ctypes.CDLL:
+    global _par
+    if _par is None:
+        build()
+        lib = ctypes.CDLL(_PAR_LIB)
+        i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+        lib.oracle_dispatch_par.argtypes = [i32, i32, i32, i32, i32, p, p, p, i64, p, p, p, p, p, p]
+        lib.oracle_dispatch_par.restype = ctypes.c_int
+        lib.oracle_combine_par.argtypes = [i32, i32, i32, p, i64, p, p, p]
+        lib.oracle_combine_par.restype = ctypes.c_int
+        lib.oracle_par_threads.argtypes = []
+        lib.oracle_par_threads.restype = ctypes.c_int
+        _par = lib
+    return _par
 
 
 def _ptr(a: Optional[np.ndarray]):
@@ -130,6 +156,48 @@ def dispatch(x: np.ndarray, topk_idx: np.ndarray, E: int, N: int,
                              _ptr(out.slot_row), _ptr(out.row_src))
     if rc != OK:
         raise OracleError(rc, "oracle_dispatch")
+    return out
+
+
+def par_threads() -> int:
+    """Threads the all-cores functions (``dispatch_par``, ``combine_par``) use."""
+    return int(_load_par().oracle_par_threads())
+
+
+def dispatch_par(x: np.ndarray, topk_idx: np.ndarray, E: int, N: int) -> Dispatch:
+    """``dispatch`` with its row copy spread over every host core
+    (``oracle_dispatch_par`` in moe_oracle_par.cc); the same bytes."""
+    lib = _load_par()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, H = x.shape
+    K = idx.shape[1]
+    rows = T * K
+    out = Dispatch(np.empty((rows, H), dtype=np.uint16), np.zeros(E, np.int32), np.zeros(E + 1, np.int32),
+                   np.zeros((E, N), np.int32), np.zeros(N + 1, np.int32),
+                   np.zeros((T, K), np.int32), np.zeros(rows, np.int32))
+    rc = lib.oracle_dispatch_par(T, H, K, E, N, _ptr(x), _ptr(idx), _ptr(out.expert_x), rows,
+                                 _ptr(out.expert_counts), _ptr(out.expert_offsets),
+                                 _ptr(out.src_offsets), _ptr(out.rank_offsets),
+                                 _ptr(out.slot_row), _ptr(out.row_src))
+    if rc != OK:
+        raise OracleError(rc, "oracle_dispatch_par")
+    return out
+
+
+def combine_par(y: np.ndarray, topk_w: np.ndarray, slot_row: np.ndarray) -> np.ndarray:
+    """``combine`` with a parallel loop over tokens (``oracle_combine_par``);
+    the same bytes."""
+    lib = _load_par()
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    sr = np.ascontiguousarray(slot_row, dtype=np.int32)
+    T, K = w.shape
+    H = y.shape[1]
+    out = np.empty((T, H), dtype=np.uint16)
+    rc = lib.oracle_combine_par(T, H, K, _ptr(y), y.shape[0], _ptr(w), _ptr(sr), _ptr(out))
+    if rc != OK:
+        raise OracleError(rc, "oracle_combine_par")
     return out
 
 
