@@ -1,5 +1,5 @@
-// moe_dispatch_send_noalloc: dispatch (route_count + dispatch_pack) for callers
-// that cannot allocate device memory.
+// moe_dispatch_send_noalloc: dispatch (route_count + the bulk dispatch_pack)
+// for callers that cannot allocate device memory.
 //
 // Some callers cannot call cudaMalloc at all: code that runs inside another
 // framework's memory pool with no allocator handle, allocation-free runtime
@@ -135,8 +135,10 @@ MOE_API int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, cons
   pp.K = cfg->top_k;
   pp.dst_rows = expert_x_rows;
   pp.row_bytes = static_cast<int64_t>(cfg->hidden) * 2;
-  // Same launch shape as moe_dispatch_send's defaults: pieces of at most
-  // 16 KiB, 4 bulk stages, as many CTAs per SM as shared memory allows.
+  // A fixed launch shape, simpler than moe_dispatch_send's automatic one (no
+  // unit queue, no L2 prefetch or cache hints, one store group in flight):
+  // pieces of at most 16 KiB, 4 bulk stages, as many CTAs per SM as shared
+  // memory allows.
   const int64_t npieces = (pp.row_bytes + 16384 - 1) / 16384;
   pp.piece_bytes = static_cast<int32_t>((pp.row_bytes / 16 + npieces - 1) / npieces * 16);
   pp.pieces = static_cast<int32_t>((pp.row_bytes + pp.piece_bytes - 1) / pp.piece_bytes);
@@ -147,8 +149,7 @@ MOE_API int moe_dispatch_send_noalloc(const moe_config* cfg, const void* x, cons
     --pl.stages;
   const size_t smem = moe::pack_bulk_smem_bytes(pl.stages, pp.piece_bytes);
   if (smem > static_cast<size_t>(ds.max_smem_optin)) return MOE_EINVAL;
-  int per_sm = static_cast<int>((228 * 1024) / (smem + 1024));
-  if (per_sm < 1) per_sm = 1;
+  const int per_sm = moe::smem_ctas_per_sm(smem);
   int64_t grid = static_cast<int64_t>(ds.num_sms) * per_sm;
   const int64_t units = static_cast<int64_t>(pp.T) * pp.pieces;
   if (grid > units) grid = units;
