@@ -540,7 +540,8 @@ def run_gpu(args):
                                    if layer.get_option(moe.MOE_OPT_COMBINE_VARIANT) == 0
                                    else "vector"),
                        "routing": {1: "route_count (1 block)", 2: "route_local+route_finalize",
-                                   3: f"route_cluster ({layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS)} CTAs)"}[
+                                   3: f"route_cluster ({layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS)} CTAs)",
+                                   4: "route_pack (routing inside the pack kernel)"}[
                            layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)]},
             "l2_warm_us": round(l2_warm_us, 2),
             "achieved_gbs": round(ab["total"] / us_layer / 1e3, 1),

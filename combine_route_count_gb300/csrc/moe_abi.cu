@@ -78,6 +78,31 @@ int resident_ctas_per_sm(const void* kernel, int threads, size_t smem) {
   return n;
 }
 
+int smem_ctas_per_sm(size_t smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  static std::mutex mu;
+  static std::map<int, std::pair<int, int>> known;  // device -> (shared memory per SM, reserve per CTA)
+  int per_sm = 0, reserve = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = known.find(dev);
+    if (it == known.end()) {
+      if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&reserve, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+      }
+      known[dev] = {per_sm, reserve};
+    } else {
+      per_sm = it->second.first;
+      reserve = it->second.second;
+    }
+  }
+  const int n = static_cast<int>(static_cast<size_t>(per_sm) / (smem + static_cast<size_t>(reserve)));
+  return n < 1 ? 1 : n;
+}
+
 }  // namespace moe
 
 namespace {
@@ -185,6 +210,7 @@ struct moe_ctx {
   int combine_stages;       // 0 = automatic
   int combine_piece_bytes;  // 0 = automatic
   int combine_ctas_per_sm;  // 0 = as many as fit
+  bool route_pack_ok;  // the one-kernel route+pack path can run this configuration
   int cluster_ctas;   // route_cluster shape for this configuration (0 = cannot be scheduled)
   int cluster_chunk;
   int cluster_warps;
@@ -239,6 +265,7 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   if (moe::route_count_smem_bytes(cfg->num_experts) > static_cast<size_t>(optin)) return MOE_EINVAL;
   if (moe::route_local_smem_bytes(cfg->num_experts) > static_cast<size_t>(optin)) return MOE_EINVAL;
   if (moe::prepare_pack(optin) != cudaSuccess) return MOE_ECUDA;
+  if (moe::prepare_route_pack(optin) != cudaSuccess) return MOE_ECUDA;
 
   moe_ctx* c = new (std::nothrow) moe_ctx;
   if (!c) return MOE_EINVAL;
@@ -283,6 +310,17 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   // fp8 layer 141.4 -> 139.0 us, Kimi-sized 545 -> 543 us, Mixtral-sized
   // unchanged).
   c->fp8_order = 1;
+  // One-kernel route+pack: small routing tables, and two stages of the
+  // automatic piece size fit next to them in one CTA.
+  {
+    const int64_t row_bytes = static_cast<int64_t>(cfg->hidden) * 2;
+    const int64_t pieces = (row_bytes + 8191) / 8192;
+    const int64_t piece = (row_bytes / 16 + pieces - 1) / pieces * 16;
+    c->route_pack_ok = moe::route_pack_eligible(cfg->num_tokens, cfg->top_k, cfg->num_experts) &&
+                       moe::route_pack_smem_bytes(cfg->num_tokens, cfg->top_k, cfg->num_experts, 1, 2,
+                                                  static_cast<int>(piece)) <=
+                           static_cast<size_t>(optin);
+  }
   // Largest cluster of route_cluster CTAs this device can schedule for this
   // configuration (16, else 8, 4, 2, 1), or none.
   for (int maxc = moe::kMaxClusterCtas; maxc >= 1; maxc /= 2) {
@@ -332,6 +370,16 @@ int pack_ctas_auto(int K) { return K >= 4 ? 2 : 3; }
 
 // SMs the persistent grids may spread over (MOE_OPT_MAX_SMS).
 int grid_sms(const moe_ctx* c) { return c->max_sms > 0 && c->max_sms < c->num_sms ? c->max_sms : c->num_sms; }
+
+// Whether moe_dispatch_send routes and packs in one kernel (route_pack):
+// forced by MOE_OPT_ROUTE_VARIANT 4, or automatic for small layers with the
+// default bulk pack and its static split.  Measured on GB300 (A/B, one box):
+// see the launch-option notes at moe_dispatch_send.
+bool dispatch_uses_route_pack(const moe_ctx* c) {
+  if (!c->route_pack_ok) return false;
+  if (c->route_variant == 4) return true;
+  return c->route_variant == 0 && c->pack_variant == moe::kPackBulk && c->pack_schedule != 1;
+}
 
 }  // namespace
 
@@ -424,8 +472,9 @@ MOE_API int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value) {
       ctx->kernel_events = static_cast<int>(value);
       return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
-      if (value < 0 || value > 3) return MOE_EINVAL;
+      if (value < 0 || value > 5) return MOE_EINVAL;
       if (value == 3 && ctx->cluster_ctas == 0) return MOE_EINVAL;
+      if ((value == 4 || value == 5) && !ctx->route_pack_ok) return MOE_EINVAL;
       ctx->route_variant = static_cast<int>(value);
       return MOE_OK;
     default:
@@ -467,7 +516,10 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
       *value = ctx->combine_schedule;
       return MOE_OK;
     case MOE_OPT_ROUTE_VARIANT:
-      *value = ctx->route_variant != 0 ? ctx->route_variant : (ctx->cluster_ctas > 0 ? 3 : 2);
+      *value = ctx->route_variant != 0    ? ctx->route_variant
+               : dispatch_uses_route_pack(ctx) ? 4
+               : ctx->cluster_ctas > 0         ? 3
+                                               : 2;
       return MOE_OK;
     case MOE_OPT_ROUTE_CLUSTER_CTAS:
       *value = ctx->cluster_ctas;
@@ -532,8 +584,7 @@ int pack_grid(const moe_ctx* c, const moe::PackParams& p, int variant, int stage
   int per_sm = c->pack_ctas_per_sm > 0 ? c->pack_ctas_per_sm : (bulk ? pack_ctas_auto(p.K) : 0);
   if (bulk) {
     const size_t smem = moe::pack_bulk_smem_bytes(stages, p.piece_bytes);
-    // 228 KiB of shared memory per SM, 1 KiB of it reserved per resident CTA.
-    const int fit = static_cast<int>((228 * 1024) / (smem + 1024));
+    const int fit = moe::smem_ctas_per_sm(smem);
     if (per_sm <= 0 || per_sm > fit) per_sm = fit;
     if (per_sm < 1) per_sm = 1;
   } else if (per_sm <= 0) {
@@ -571,9 +622,38 @@ int enqueue_routing(moe_ctx* ctx, const int32_t* topk_idx, cudaStream_t s) {
   int vec = 1;
   if (c.top_k % 4 == 0 && aligned(topk_idx, 16)) vec = 4;
   else if (c.top_k % 2 == 0 && aligned(topk_idx, 8)) vec = 2;
-  const bool use_cluster = (ctx->route_variant == 0 || ctx->route_variant == 3) && ctx->cluster_ctas > 0;
+  // Variant 4 (one-kernel route+pack) exists only for moe_dispatch_send;
+  // every other dispatch form routes as in the automatic choice.
+  const bool use_cluster =
+      (ctx->route_variant == 0 || ctx->route_variant == 3 || ctx->route_variant == 4) && ctx->cluster_ctas > 0;
   if (ctx->route_variant == 1) {
     if (moe::launch_route_count(rp, vec, s) != cudaSuccess) return MOE_ECUDA;
+  } else if (ctx->route_variant == 5 && c.num_tokens > 0) {
+    // route_pack's routing alone, in one CTA (no copy warps).
+    moe::RoutePackParams qp = {};
+    qp.topk_idx = topk_idx;
+    qp.T = c.num_tokens;
+    qp.K = c.top_k;
+    qp.E = c.num_experts;
+    qp.N = c.num_ranks;
+    qp.row_bytes = 16;
+    qp.piece_bytes = 16;
+    qp.pieces = 1;
+    qp.expert_counts = ctx->expert_counts;
+    qp.expert_offsets = ctx->expert_offsets;
+    qp.src_offsets = ctx->src_offsets;
+    qp.rank_offsets = ctx->rank_offsets;
+    qp.slot_row = ctx->slot_row;
+    qp.row_src = ctx->row_src;
+    qp.error_word = ctx->error_word;
+    qp.queue = ctx->queue;
+    moe::RoutePackLaunch ql = {};
+    ql.grid = 1;
+    ql.copy_warps = 0;
+    ql.stages = 2;
+    ql.depth = 1;
+    ql.pdl = ctx->pdl != 0;
+    if (moe::launch_route_pack(qp, ql, s) != cudaSuccess) return MOE_ECUDA;
   } else if (use_cluster) {
     moe::RouteClusterParams cp = {};
     cp.topk_idx = topk_idx;
@@ -706,6 +786,67 @@ int enqueue_pack(moe_ctx* ctx, const void* src, void* dst, int64_t dst_rows, con
 
 }  // namespace
 
+namespace {
+
+// Enqueues route_pack: routing and the bulk pack of x into expert_x in one
+// kernel (moe_dispatch_send of a small layer), one CTA per SM.  Its copy
+// warps stand for the two-kernel path's static bulk-pack CTAs: as many per SM
+// (MOE_OPT_PACK_CTAS_PER_SM, else 2 for K >= 4 and 3 otherwise), the same
+// pieces, stage budget (about 200 KiB per SM), cache hints and store depth;
+// the stages shrink until everything fits next to the routing tables.
+// MOE_OK, MOE_EINVAL or MOE_ECUDA.
+int enqueue_route_pack(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_x, int64_t expert_x_rows,
+                       cudaStream_t s) {
+  const moe_config& c = ctx->cfg;
+  moe::RoutePackParams rp = {};
+  rp.topk_idx = topk_idx;
+  rp.x = static_cast<const uint8_t*>(x);
+  rp.expert_x = static_cast<uint8_t*>(expert_x);
+  rp.T = c.num_tokens;
+  rp.K = c.top_k;
+  rp.E = c.num_experts;
+  rp.N = c.num_ranks;
+  rp.row_bytes = static_cast<int64_t>(c.hidden) * 2;
+  const int64_t dest_bytes = static_cast<int64_t>(c.num_tokens) * c.top_k * rp.row_bytes;
+  rp.piece_bytes = pack_piece_bytes(ctx, rp.row_bytes, dest_bytes);
+  rp.pieces = static_cast<int32_t>((rp.row_bytes + rp.piece_bytes - 1) / rp.piece_bytes);
+  rp.dst_rows = expert_x_rows;
+  rp.expert_counts = ctx->expert_counts;
+  rp.expert_offsets = ctx->expert_offsets;
+  rp.src_offsets = ctx->src_offsets;
+  rp.rank_offsets = ctx->rank_offsets;
+  rp.slot_row = ctx->slot_row;
+  rp.row_src = ctx->row_src;
+  rp.error_word = ctx->error_word;
+  rp.queue = ctx->queue;
+
+  moe::RoutePackLaunch rl = {};
+  int warps = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : pack_ctas_auto(c.top_k);
+  if (warps > moe::kRoutePackThreads / 32) warps = moe::kRoutePackThreads / 32;
+  auto smem_of = [&](int w, int st) { return moe::route_pack_smem_bytes(rp.T, rp.K, rp.E, w, st, rp.piece_bytes); };
+  while (warps > 1 && smem_of(warps, 2) > static_cast<size_t>(ctx->max_smem_optin)) --warps;
+  int stages = ctx->pack_stages > 0 ? ctx->pack_stages : static_cast<int>((200 * 1024) / warps / rp.piece_bytes);
+  const int maxst = moe::route_pack_max_stages(warps);
+  if (stages > maxst) stages = maxst;
+  if (stages < 2) stages = 2;
+  while (stages > 2 && smem_of(warps, stages) > static_cast<size_t>(ctx->max_smem_optin)) --stages;
+  if (smem_of(warps, stages) > static_cast<size_t>(ctx->max_smem_optin)) return MOE_EINVAL;
+  const int64_t units = static_cast<int64_t>(rp.T) * rp.pieces;
+  int64_t grid = (units + warps - 1) / warps;
+  if (grid > grid_sms(ctx)) grid = grid_sms(ctx);
+  if (grid < 1) grid = 1;
+  rl.grid = static_cast<int>(grid);
+  rl.copy_warps = warps;
+  rl.stages = stages;
+  rl.hints = ctx->cache_hints;
+  rl.depth = ctx->pack_depth > 0 ? ctx->pack_depth : 2;
+  rl.pdl = ctx->pdl != 0;
+  if (moe::launch_route_pack(rp, rl, s) != cudaSuccess) return MOE_ECUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
 MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_x,
                               int64_t expert_x_rows, void* stream) {
   NvtxRange nvtx_range("moe_dispatch_send");
@@ -719,6 +860,16 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     if (!aligned(x, 16) || !aligned(expert_x, 16) || !aligned(topk_idx, 4)) return MOE_EINVAL;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c.num_tokens > 0 && dispatch_uses_route_pack(ctx)) {
+    const bool timed = ctx->kernel_events != 0;
+    if (timed && cudaEventRecord(ctx->ev[0], s) != cudaSuccess) return MOE_ECUDA;
+    const int frc = enqueue_route_pack(ctx, x, topk_idx, expert_x, expert_x_rows, s);
+    if (frc != MOE_OK) return frc;
+    if (timed && cudaEventRecord(ctx->ev[1], s) != cudaSuccess) return MOE_ECUDA;
+    ctx->pack_timed = timed;
+    ctx->phase = kDispatched;
+    return MOE_OK;
+  }
   const int rrc = enqueue_routing(ctx, topk_idx, s);
   if (rrc != MOE_OK) return rrc;
 
@@ -870,7 +1021,7 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
     while (stages > 2 && moe::pack_fp8_smem_bytes(stages, c.hidden) > static_cast<size_t>(ctx->max_smem_optin))
       --stages;
     const size_t smem = moe::pack_fp8_smem_bytes(stages, c.hidden);
-    int per_sm = static_cast<int>((228 * 1024) / (smem + 1024));
+    int per_sm = moe::smem_ctas_per_sm(smem);
     const int want = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : (few_dest ? 8 : 3);
     if (per_sm > want) per_sm = want;
     if (per_sm < 1) per_sm = 1;
@@ -978,7 +1129,7 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
       if (cl.shape.queue) cp.queue = ctx->queue + 1;
       const size_t smem = moe::combine_bulk_smem_bytes(cl.shape, c.top_k);
       if (smem > static_cast<size_t>(ctx->max_smem_optin)) return MOE_EINVAL;
-      const int fit = static_cast<int>((228 * 1024) / (smem + 1024));
+      const int fit = moe::smem_ctas_per_sm(smem);
       int per_sm = ctx->combine_ctas_per_sm > 0 && ctx->combine_ctas_per_sm < fit ? ctx->combine_ctas_per_sm : fit;
       if (per_sm < 1) per_sm = 1;
       const int64_t units = static_cast<int64_t>(c.num_tokens) * cl.shape.pieces;

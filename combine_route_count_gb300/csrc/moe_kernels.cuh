@@ -89,6 +89,45 @@ bool route_cluster_supported(const RouteClusterParams& p, int idx_vec, int clust
 cudaError_t launch_route_cluster(const RouteClusterParams& p, int idx_vec, int cluster, cudaStream_t stream);
 
 // ---- dispatch_pack: expert_x[slot_row[t,k]] = x[t] --------------------------
+// Routing and pack in one kernel, for small layers (route_pack.cu): one CTA
+// per SM computes the whole routing from topk_idx in shared memory, then
+// `copy_warps` of its warps each copy units through their own stage ring.
+constexpr int kRoutePackThreads = 1024;
+constexpr int kRoutePackMaxPairs = 16384;     // T*K: index reads per CTA
+constexpr int kRoutePackMaxMaskWords = 4096;  // E*ceil(T/32): token-mask words per CTA
+struct RoutePackParams {
+  const int32_t* topk_idx;  // [T, K]
+  const uint8_t* x;         // [T, row_bytes]
+  uint8_t* expert_x;        // [dst_rows, row_bytes]
+  int32_t T, K, E, N;
+  int64_t row_bytes;        // multiple of 16
+  int32_t piece_bytes;      // bytes moved per unit (multiple of 16, <= row_bytes)
+  int32_t pieces;           // ceil(row_bytes / piece_bytes)
+  int64_t dst_rows;         // rows of expert_x (checked builds)
+  int32_t* expert_counts;   // [E]
+  int32_t* expert_offsets;  // [E+1]
+  int32_t* src_offsets;     // [E*N]
+  int32_t* rank_offsets;    // [N+1]
+  int32_t* slot_row;        // [T*K]
+  int32_t* row_src;         // [T*K]
+  int32_t* error_word;      // [1]
+  unsigned long long* queue;  // [2] the pack's and the combine's queues: set to 0 here (may be null)
+};
+struct RoutePackLaunch {
+  int grid;        // CTAs (at most one per SM)
+  int copy_warps;  // warps per CTA that copy, each a virtual pack CTA (1..8)
+  int stages;      // shared-memory stages per copy warp (2..route_pack_max_stages)
+  int hints;   // CacheHints
+  int depth;   // store groups in flight before a stage is refilled
+  bool pdl;    // launch with programmatic stream serialization
+};
+size_t route_pack_tables_bytes(int T, int E);
+size_t route_pack_smem_bytes(int T, int K, int E, int copy_warps, int stages, int piece_bytes);
+int route_pack_max_stages(int copy_warps);
+bool route_pack_eligible(int T, int K, int E);
+cudaError_t prepare_route_pack(int max_smem_bytes);  // one-time per-device attribute setup
+cudaError_t launch_route_pack(const RoutePackParams& p, const RoutePackLaunch& l, cudaStream_t stream);
+
 struct PackParams {
   const uint8_t* x;         // [T, row_bytes]
   uint8_t* expert_x;        // [rows, row_bytes]
@@ -211,6 +250,11 @@ cudaError_t set_kernel_limits(const void* kernel, size_t bytes, bool nonportable
 // CTAs of `kernel` that can be resident on one SM with this block size and
 // dynamic shared memory (0 if the query fails); cached per device.
 int resident_ctas_per_sm(const void* kernel, int threads, size_t smem);
+
+// CTAs with `smem` bytes of dynamic shared memory that fit on one SM of the
+// current device (its shared memory per SM over smem plus the per-CTA
+// reserve); at least 1, cached per device.
+int smem_ctas_per_sm(size_t smem);
 
 // Launch helper: plain or programmatic-dependent launch with cudaLaunchKernelEx.
 template <typename... KArgs, typename... Args>

@@ -24,7 +24,7 @@ MOE_MAX_TOP_K = 16
 MOE_MAX_EXPERTS = 1024
 (MOE_OPT_PACK_VARIANT, MOE_OPT_PACK_STAGES, MOE_OPT_PACK_PIECE_BYTES, MOE_OPT_PACK_CTAS_PER_SM, MOE_OPT_PDL,
  MOE_OPT_ROUTE_VARIANT, MOE_OPT_ROUTE_CLUSTER_CTAS) = 1, 2, 3, 4, 5, 6, 7
-ROUTE_AUTO, ROUTE_SINGLE, ROUTE_SPLIT, ROUTE_CLUSTER = 0, 1, 2, 3
+ROUTE_AUTO, ROUTE_SINGLE, ROUTE_SPLIT, ROUTE_CLUSTER, ROUTE_FUSED = 0, 1, 2, 3, 4
 MOE_OPT_COMBINE_VARIANT, MOE_OPT_COMBINE_STAGES, MOE_OPT_COMBINE_PIECE_BYTES, MOE_OPT_COMBINE_CTAS_PER_SM = 8, 9, 10, 11
 COMBINE_BULK, COMBINE_VECTOR = 0, 1
 MOE_OPT_PACK_PREFETCH = 12
@@ -366,6 +366,8 @@ class MoELayer:
     def kernels_per_layer(self) -> int:
         """Kernel launches of one dispatch+combine layer (T > 0)."""
         route = self.get_option(MOE_OPT_ROUTE_VARIANT)
+        if route == ROUTE_FUSED:
+            return 2  # route_pack, combine
         return (2 if route == ROUTE_SPLIT else 1) + 2
 
     def dispatch_send(self, x, topk_idx, expert_x, stream: Any = None) -> None:

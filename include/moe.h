@@ -122,7 +122,10 @@ int moe_ctx_destroy(moe_ctx* ctx);
  * routing error check: by default route_cluster, one thread-block cluster of
  * up to 16 CTAs that exchange per-chunk counts through distributed shared
  * memory; see MOE_OPT_ROUTE_VARIANT) and dispatch_pack (copies each token row
- * x[t] to expert_x[slot_row[t,k]] for every k).
+ * x[t] to expert_x[slot_row[t,k]] for every k).  For small layers (T*K <=
+ * 16384, E*ceil(T/32) <= 4096) both run as one kernel, route_pack, whose CTAs
+ * each compute the routing tables before copying: one kernel boundary less
+ * on the layer's critical path.  The results are the same either way.
  *   x         device bf16 [T, H], read only
  *   topk_idx  device int32 [T, K], read only, 4-byte aligned
  *   expert_x  device bf16 [expert_x_rows, H]; rows [0, T*K) are written,
@@ -259,12 +262,21 @@ int moe_partial_rows(const moe_config* cfg, int64_t* rows);
  *                             fp8 pack: 3 for K >= 4, else up to 8), else 1..32
  *   MOE_OPT_PDL               1 = launch pack/combine with programmatic
  *                             dependent launch (default), 0 = plain launches
- *   MOE_OPT_ROUTE_VARIANT     routing kernels: 0 = automatic (route_cluster
- *                             when the device can schedule its cluster, else
+ *   MOE_OPT_ROUTE_VARIANT     routing kernels: 0 = automatic (for
+ *                             moe_dispatch_send of a small layer, 4 when the
+ *                             bulk pack and its automatic or static split are
+ *                             selected; otherwise route_cluster when the
+ *                             device can schedule its cluster, else
  *                             route_local + route_finalize), 1 = the
  *                             single-block route_count, 2 = route_local +
  *                             route_finalize, 3 = route_cluster (MOE_EINVAL
- *                             if the device cannot schedule it) */
+ *                             if the device cannot schedule it), 4 =
+ *                             route_pack: moe_dispatch_send routes and packs
+ *                             in one kernel, every CTA of the pack grid
+ *                             computing the routing tables itself (bulk
+ *                             copies, static split; MOE_EINVAL unless
+ *                             T*K <= 16384 and E*ceil(T/32) <= 4096; the
+ *                             other dispatch calls route as with 0) */
 #define MOE_OPT_PACK_VARIANT 1
 #define MOE_OPT_PACK_STAGES 2
 #define MOE_OPT_PACK_PIECE_BYTES 3
@@ -274,7 +286,7 @@ int moe_partial_rows(const moe_config* cfg, int64_t* rows);
 int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
 
 /* Reads back a launch option.  For MOE_OPT_ROUTE_VARIANT set to 0
- * (automatic) it reports the path dispatch will take (2 or 3);
+ * (automatic) it reports the path moe_dispatch_send will take (2, 3 or 4);
  * MOE_OPT_ROUTE_CLUSTER_CTAS reports the route_cluster cluster size chosen
  * for this configuration (0 if the device cannot schedule it). */
 #define MOE_OPT_ROUTE_CLUSTER_CTAS 7
@@ -394,10 +406,13 @@ int moe_kernel_times(moe_ctx* ctx, float* pack_ms, float* combine_ms);
  * processes that may not grow their device footprint after start-up), so
  * they cannot provide the workspace that moe_ctx_create needs.
  *
- * Does what moe_dispatch_send does (route_count + dispatch_pack, same
- * kernels, same results) but keeps the routing tables in one fixed static
- * device array inside the library (MOE_NOALLOC_SCRATCH_BYTES, held by every
- * GPU that loads libmoe.so until the process exits) and allocates nothing.
+ * Gives the same results as moe_dispatch_send (the same grouped rows, counts
+ * and offsets) but routes with the single-block route_count kernel (slower
+ * than moe_dispatch_send's default routing on large layers) and packs with
+ * the bulk pack's static split; it keeps the routing tables in one fixed
+ * static device array inside the library (MOE_NOALLOC_SCRATCH_BYTES, held by
+ * every GPU that loads libmoe.so until the process exits) and allocates
+ * nothing.
  *   x, topk_idx, expert_x, expert_x_rows  as for moe_dispatch_send
  *   expert_counts   device int32 [E], written
  *   expert_offsets  device int32 [E+1], written

@@ -432,7 +432,7 @@ def test_repeat_runs_are_byte_identical(moe):
     w = gen.custom("det", T=2048, H=1024, K=8, E=64, N=8, seed_index=5)
     li = gen.make_inputs(w)
     first = run_gpu(moe, w, li)
-    for _ in range(3):
+    for _ in range(10):
         again = run_gpu(moe, w, li)
         for k in ("expert_x", "out", "slot_row", "row_src", "expert_offsets", "src_offsets"):
             assert np.array_equal(first[k], again[k]), k
@@ -466,3 +466,106 @@ def test_kernel_events_time_both_kernels_and_keep_results(moe, oracle_mod):
     assert layer.get_error() == 0
     with pytest.raises(moe.MoEError):
         layer.set_option(moe.MOE_OPT_KERNEL_EVENTS, 2)
+
+
+ROUTE_PACK_OPTIONS = [
+    dict(),
+    dict(pack_stages=2, pack_store_depth=1),
+    dict(pack_piece_bytes=1024, pack_ctas_per_sm=1, pack_stages=16),
+    dict(pdl=0, cache_hints=0),
+    dict(pack_store_depth=5, pack_stages=6, combine_variant=0, combine_schedule=1),
+]
+ROUTE_PACK_SHAPES = [s for s in EDGE if s[0] * s[2] <= 16384 and (s[0] + 31) // 32 * s[3] <= 4096] + [
+    (4000, 4104, 4, 32, 8, "uniform_random"),   # two pieces per row, many units per CTA
+    (2048, 512, 8, 64, 8, "uniform_random"),    # at both limits: T*K = 16384, E*ceil(T/32) = 4096
+    (1024, 64, 4, 16, 4, "rank0_only"),         # every token to rank 0
+]
+
+
+@pytest.mark.parametrize("route", [4, 5], ids=["in-pack", "one-cta"])
+@pytest.mark.parametrize("opts", ROUTE_PACK_OPTIONS, ids=[str(o) for o in ROUTE_PACK_OPTIONS])
+@pytest.mark.parametrize("shape", ROUTE_PACK_SHAPES, ids=["x".join(map(str, s[:5])) for s in ROUTE_PACK_SHAPES])
+def test_route_pack_shapes_and_options(moe, oracle_mod, shape, opts, route):
+    """Routing inside the pack kernel (route variant 4), or the same routing
+    alone in one CTA ahead of the pack (variant 5): every table and row
+    bit-exact, nothing written outside the outputs."""
+    T, H, K, E, N, router = shape
+    w = gen.custom("fused", T=T, H=H, K=K, E=E, N=N, router=router, seed_index=61)
+    li = gen.make_inputs(w)
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    res = run_gpu(moe, w, li, extra_rows=4, route_variant=route, **opts)
+    assert res["layer"].kernels_per_layer() == (2 if route == 4 else 3)
+    assert_parity(res, d, out_ref, w, extra_rows=4)
+
+
+def test_route_pack_is_the_automatic_choice_for_small_layers_only(moe):
+    small = moe.MoELayer(4096, 4096, 2, 8, 8)  # Mixtral-sized
+    assert small.get_option(moe.MOE_OPT_ROUTE_VARIANT) == moe.ROUTE_FUSED
+    assert small.kernels_per_layer() == 2
+    small.set_option(moe.MOE_OPT_PACK_SCHEDULE, 1)  # the unit queue is a two-kernel feature
+    assert small.get_option(moe.MOE_OPT_ROUTE_VARIANT) == moe.ROUTE_CLUSTER
+    small.set_option(moe.MOE_OPT_PACK_SCHEDULE, -1)
+    small.set_option(moe.MOE_OPT_PACK_VARIANT, moe.PACK_VECTOR)
+    assert small.get_option(moe.MOE_OPT_ROUTE_VARIANT) == moe.ROUTE_CLUSTER
+    big = moe.MoELayer(4096, 7168, 8, 256, 32)  # DeepSeek-sized: T*K = 32768
+    assert big.get_option(moe.MOE_OPT_ROUTE_VARIANT) == moe.ROUTE_CLUSTER
+    with pytest.raises(moe.MoEError) as ei:
+        big.set_option(moe.MOE_OPT_ROUTE_VARIANT, moe.ROUTE_FUSED)
+    assert ei.value.code == moe.MOE_EINVAL
+    with pytest.raises(moe.MoEError):
+        small.set_option(moe.MOE_OPT_ROUTE_VARIANT, 6)
+
+
+@pytest.mark.parametrize("route", [4, 5], ids=["in-pack", "one-cta"])
+@pytest.mark.parametrize("bad", ["out_of_range", "negative", "repeated"])
+def test_route_pack_routing_errors_write_nothing(moe, bad, route):
+    w = gen.custom("bad", T=300, H=64, K=4, E=16, N=4, seed_index=3)
+    li = gen.make_inputs(w)
+    idx = li.topk_idx.copy()
+    if bad == "out_of_range":
+        idx[123, 2] = 16
+    elif bad == "negative":
+        idx[7, 0] = -1
+    else:
+        idx[299, 3] = idx[299, 1]
+    li2 = gen.LayerInputs(w, li.x, idx, li.topk_w, li.y)
+    res = run_gpu(moe, w, li2, route_variant=route, combine_variant=0)
+    assert res["status"] == moe.MOE_EROUTE
+    assert res["guards_ok"]
+    assert np.all(res["expert_x"] == CANARY)
+    assert np.all(res["out"] == CANARY)
+    assert np.all(res["slot_row"] == -1)
+    assert np.all(res["expert_counts"] == 0) and np.all(res["expert_offsets"] == 0)
+    assert np.all(res["src_offsets"] == 0) and np.all(res["rank_offsets"] == 0)
+    layer = res["layer"]
+    T, H, K = w.T, w.H, w.K
+    ex = torch.empty((T * K, H), dtype=torch.int16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    layer.layer(_dev(li.x.view(np.int16)), _dev(li.topk_idx), _dev(li.topk_w), ex, _dev(li.y.view(np.int16)), out)
+    assert layer.get_error() == moe.MOE_OK
+
+
+def test_route_pack_resets_the_combine_queue_every_layer(moe, oracle_mod):
+    """Layers with different routings on one context, routing inside the pack
+    and the bulk combine's token queue on: the pack kernel resets the queue
+    each layer, also across a routing error and a two-kernel layer."""
+    T, H, K, E, N = 1024, 1024, 8, 32, 8
+    layer = moe.MoELayer(T, H, K, E, N, combine_variant=0, combine_schedule=1)
+    ex = torch.empty((T * K, H), dtype=torch.int16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    for n, route in enumerate([4, 4, 3, 4, 5, 0, 5, 4]):
+        w = gen.custom("queue", T=T, H=H, K=K, E=E, N=N, router="uniform_random", seed_index=70 + n)
+        li = gen.make_inputs(w)
+        d, out_ref = oracle_of(oracle_mod, w, li)
+        x, idx, wt, y = (_dev(li.x.view(np.int16)), _dev(li.topk_idx), _dev(li.topk_w), _dev(li.y.view(np.int16)))
+        layer.set_option(moe.MOE_OPT_ROUTE_VARIANT, route)
+        if n == 3:
+            bad = li.topk_idx.copy()
+            bad[9, 5] = bad[9, 0]
+            layer.layer(x, _dev(bad), wt, ex, y, out)
+            assert layer.get_error() == moe.MOE_EROUTE
+        lay = layer.layer(x, idx, wt, ex, y, out)
+        assert layer.get_error() == 0
+        assert np.array_equal(lay["slot_row"].cpu().numpy(), d.slot_row)
+        assert np.array_equal(ex.cpu().numpy().view(np.uint16), d.expert_x), n
+        assert np.array_equal(out.cpu().numpy().view(np.uint16), out_ref), n
