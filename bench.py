@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--workload", default="deepseek")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only the headline workload (not the other workloads of the benchmark)")
     ap.add_argument("--buffer-sets", type=int, default=2)
     ap.add_argument("--payload", choices=["bf16", "fp8", "fp8q"], default="bf16",
                     help="dispatch payload: bf16 rows, or block-scaled fp8 rows (moe_dispatch_send_fp8)")
@@ -231,20 +233,36 @@ def run_reference(args):
     }), flush=True)
 
 
-def cpu_baseline(w, li, budget_s=10.0, max_reps=100):
-    """The oracle timed on one host core over the full layer, repeated."""
-    import oracle
-    oracle.build()
+def _time_oracle_layer(dispatch_fn, combine_fn, w, li, budget_s, max_reps):
     times = []
     t_end = time.perf_counter() + budget_s
     while len(times) < max_reps and (not times or time.perf_counter() < t_end):
         t0 = time.perf_counter()
-        d = oracle.dispatch(li.x, li.topk_idx, w.E, w.N)
-        oracle.combine(li.y, li.topk_w, d.slot_row)
+        d = dispatch_fn(li.x, li.topk_idx, w.E, w.N)
+        combine_fn(li.y, li.topk_w, d.slot_row)
         times.append(time.perf_counter() - t0)
-    us = statistics.mean(times) * 1e6
-    return {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"full {w.name} layer (dispatch + combine) x{len(times)}, single-threaded"}
+    return statistics.mean(times) * 1e6, len(times)
+
+
+def cpu_baseline(w, li, budget_s=8.0, max_reps=100):
+    """The oracle on this host over the full layer, repeated: its loops
+    spread over every core this process may use (OpenMP, the headline
+    value), and as it stands on one core, in the same run."""
+    import oracle
+    oracle.build()
+    threads = oracle.par_threads()
+    us_par, n_par = _time_oracle_layer(oracle.dispatch_par, oracle.combine_par, w, li, budget_s, max_reps)
+    us_one, n_one = _time_oracle_layer(oracle.dispatch, oracle.combine, w, li, budget_s, max_reps)
+    try:
+        affinity = len(os.sched_getaffinity(0))
+    except AttributeError:
+        affinity = None
+    return {"value": round(us_par, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"full {w.name} layer (dispatch + combine) x{n_par}, the oracle's loops over {threads} "
+                      f"threads (OpenMP: grouped-row copy and per-token combine in parallel)",
+            "single_thread": {"value": round(us_one, 1), "unit": UNIT, "cores": 1,
+                              "sample": f"full {w.name} layer x{n_one}, the oracle as it stands"},
+            "host_cpus": os.cpu_count(), "host_cpus_usable": affinity}
 
 
 def run_gpu(args):
@@ -509,6 +527,28 @@ def run_gpu(args):
     if not args.no_e2e and args.payload == "bf16" and args.combine == "receiver" and args.dispatch == "direct":
         e2e = run_e2e(args, w, li, layer, stream, dev)
 
+    workloads = None
+    if not args.no_workloads and ws == 1 and args.payload == "bf16" and args.dispatch == "direct" \
+            and args.combine == "receiver" and not args.graph:
+        # Every workload of the benchmark in the same run; "frac" uses the
+        # faster of direct calls and graph replay.
+        wclocks = ClockSampler(torch.cuda.current_device()).start()
+        time.sleep(0.2)
+        t_w0 = time.time()
+        workloads = {w.name: {"us": round(us_layer, 2), "bytes": ab["total"], "steps": args.steps,
+                              "tbs": round(ab["total"] / us_layer / 1e6, 3),
+                              "frac": round(ab["total"] / us_layer / 1e3 / peak, 4), "payload": "bf16",
+                              "note": "the headline line"}}
+        for name, payload, n in EXTRA_WORKLOADS:
+            key = name if payload == "bf16" else f"{name}_{payload}"
+            if key == w.name:
+                continue
+            workloads[key] = time_workload(name, payload, max(n, min(args.steps, 4 * n)), dev, peak)
+        workloads["clocks"] = wclocks.stop(t_w0, time.time())
+        workloads["method"] = ("two rotating buffer sets, one pair of CUDA events around `steps` layers; us: direct "
+                               "C-ABI calls from Python, us_graph: the same calls replayed from a CUDA graph; frac: "
+                               "algorithmic bytes / the faster of the two / measured copy peak")
+
     cpu = None
     if not args.no_cpu and rank == 0:
         cpu = cpu_baseline(w, li)
@@ -549,6 +589,7 @@ def run_gpu(args):
             "algorithmic_bytes_per_layer": ab["total"],
             "kernels": kernels,
             "roofline": roofline,
+            "workloads": workloads,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "clocks": clk,
@@ -560,6 +601,97 @@ def run_gpu(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# The other workloads of the benchmark, timed in the same run with the
+# headline's method (two rotating buffer sets, one pair of CUDA events around
+# K layers); the DeepSeek-sized layer also with the fp8 dispatch payload.
+# Steps per workload: at least ~20 ms of timed layers.
+EXTRA_WORKLOADS = [("tiny", "bf16", 4000), ("mixtral", "bf16", 1000), ("kimi", "bf16", 60), ("worst", "bf16", 120),
+                   ("deepseek", "fp8", 300)]
+
+
+def time_workload(name, payload, steps, dev, peak, warmup=10):
+    """µs per layer of one workload: direct C-ABI calls (what the headline
+    times) and the same calls replayed from a CUDA graph (no host work per
+    layer).  Token rows and routing from the seeded generator; the
+    synthetic expert outputs are drawn on the device (their values do not
+    change the work)."""
+    import numpy as np
+    import torch
+
+    from combine_route_count_gb300 import inputs as gen
+    from combine_route_count_gb300 import moe
+    w = gen.BY_NAME[name]
+    li = gen.make_inputs(w, with_y=False)
+    T, H, K, E, N = w.T, w.H, w.K, w.E, w.N
+    stream = torch.cuda.Stream(device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    with torch.cuda.stream(stream):
+        x0 = torch.from_numpy(li.x.view(np.int16)).to(dev)
+        idx0 = torch.from_numpy(li.topk_idx).to(dev)
+        w0 = torch.from_numpy(li.topk_w).to(dev)
+        y0 = torch.randn((T * K, H), generator=g, device=dev, dtype=torch.bfloat16).view(torch.int16)
+        sets = []
+        for _ in range(2):
+            sets.append(dict(x=x0.clone(), idx=idx0.clone(), w=w0.clone(), y=y0.clone(),
+                             ex=torch.empty((T * K, H), dtype=torch.int16 if payload == "bf16" else torch.uint8,
+                                            device=dev),
+                             xs=None if payload == "bf16" else torch.empty((T * K, H // 128), dtype=torch.float32,
+                                                                           device=dev),
+                             out=torch.empty((T, H), dtype=torch.int16, device=dev)))
+        del x0, idx0, w0, y0
+    torch.cuda.synchronize(dev)
+    layer = moe.MoELayer(T, H, K, E, N, device=dev)
+
+    def step(s_):
+        if payload == "bf16":
+            layer.dispatch_send(s_["x"], s_["idx"], s_["ex"], stream)
+        else:
+            layer.dispatch_send_fp8(s_["x"], s_["idx"], s_["ex"], s_["xs"], stream)
+        layer.dispatch_recv(stream)
+        layer.combine_send(s_["y"], stream)
+        layer.combine_recv(s_["w"], s_["out"], stream)
+
+    for i in range(warmup):
+        step(sets[i % 2])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(steps):
+        step(sets[i % 2])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) / steps * 1e3
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for s_ in sets:
+            step(s_)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps // 2):
+            graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us_graph = e0.elapsed_time(e1) / (2 * (steps // 2)) * 1e3
+    status = layer.get_error(stream)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device reported status {status} timing {name}")
+    routing = {1: "route_count", 2: "route_local+route_finalize", 3: "route_cluster", 4: "route_pack (in the pack)",
+               5: "route_pack (one CTA)"}[layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)]
+    layer.close()
+    del sets, graph
+    torch.cuda.empty_cache()
+    ab = algorithmic_bytes(w, payload)["total"]
+    best = min(us, us_graph)
+    return {"us": round(us, 2), "us_graph": round(us_graph, 2), "bytes": ab, "steps": steps,
+            "tbs": round(ab / best / 1e6, 3), "frac": round(ab / best / 1e3 / peak, 4),
+            "payload": payload, "routing": routing}
 
 
 def run_e2e(args, w, li, layer, stream, dev):
