@@ -92,7 +92,7 @@ cudaError_t launch_route_cluster(const RouteClusterParams& p, int idx_vec, int c
 // Routing and pack in one kernel, for small layers (route_pack.cu): one CTA
 // per SM computes the whole routing from topk_idx in shared memory, then
 // `copy_warps` of its warps each copy units through their own stage ring.
-constexpr int kRoutePackThreads = 1024;
+constexpr int kRoutePackThreads = 1024;  // largest block; 256 for layers of at most 32 token words
 constexpr int kRoutePackMaxPairs = 16384;     // T*K: index reads per CTA
 constexpr int kRoutePackMaxMaskWords = 4096;  // E*ceil(T/32): token-mask words per CTA
 struct RoutePackParams {
@@ -115,7 +115,8 @@ struct RoutePackParams {
 };
 struct RoutePackLaunch {
   int grid;        // CTAs (at most one per SM)
-  int copy_warps;  // warps per CTA that copy, each a virtual pack CTA (1..8)
+  int threads;     // block size: 256 or kRoutePackThreads (a multiple of 32, >= 32 * copy_warps)
+  int copy_warps;  // warps per CTA that copy, each a virtual pack CTA (0..8; 0: routing only)
   int stages;      // shared-memory stages per copy warp (2..route_pack_max_stages)
   int hints;   // CacheHints
   int depth;   // store groups in flight before a stage is refilled

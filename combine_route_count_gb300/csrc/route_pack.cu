@@ -462,7 +462,10 @@ cudaError_t launch_route_pack(const RoutePackParams& p, const RoutePackLaunch& l
   const int stages = l.stages < 2 ? 2 : (l.stages > maxst ? maxst : l.stages);
   const size_t smem = route_pack_smem_bytes(p.T, p.K, p.E, l.copy_warps, stages, p.piece_bytes);
   const int depth = clamp_depth(l.depth, stages);
-  const dim3 grid(l.grid), block(kRoutePackThreads);
+  const int threads = l.threads >= 32 * (l.copy_warps > 1 ? l.copy_warps : 1) && l.threads <= kRoutePackThreads
+                          ? l.threads / 32 * 32
+                          : kRoutePackThreads;
+  const dim3 grid(l.grid), block(threads);
   if (p.K <= 2)
     return launch_kernel(route_pack_kernel<2>, grid, block, smem, stream, l.pdl, p, l.copy_warps, stages, l.hints,
                          depth);
