@@ -37,24 +37,26 @@ __device__ __forceinline__ void fma_word(uint32_t word, float w, float& acc_lo, 
 
 constexpr int kThreads = 256;
 
-// Flat mapping: thread g handles 16-byte chunk c = g % C of token t = g / C
-// (C = H / 8 chunks per row), so a warp reads 512 contiguous bytes of each of
-// its K gathered rows.  MIN_BLOCKS sets the register budget: all K loads are
-// live at once (4 registers each).
-template <int KMAX, int MIN_BLOCKS>
+// Flat mapping: thread g handles CPT 16-byte chunks c0, c0 + C/CPT, ... of
+// token t = g / (C/CPT), c0 = g % (C/CPT) (C = H / 8 chunks per row), so a
+// warp reads 512 contiguous bytes of each of its K gathered rows per chunk
+// step, and a thread keeps CPT*K loads in flight behind one read of the
+// token's slot rows.  MIN_BLOCKS sets the register budget: all CPT*K loads
+// are live at once (4 registers each).
+template <int KMAX, int MIN_BLOCKS, int CPT>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) combine_kernel(CombineParams p) {
   ptx::wait_prerequisites();
   const int K = p.K;
-  const int64_t C = p.H >> 3;
+  const int64_t CT = (p.H >> 3) / CPT;  // threads per token
   const int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  if (g >= static_cast<int64_t>(p.T) * C) return;
-  const int64_t t = g / C;
-  const int64_t c = g - t * C;
+  if (g >= static_cast<int64_t>(p.T) * CT) return;
+  const int64_t t = g / CT;
+  const int64_t c0 = g - t * CT;
   const int64_t row_bytes = static_cast<int64_t>(p.H) * 2;
   const int32_t* slots = p.slot_row + t * K;
 
   int bad = 0;
-  uint4 v[KMAX];
+  uint4 v[CPT][KMAX];
 #pragma unroll
   for (int k = 0; k < KMAX; ++k) {
     if (k < K) {
@@ -62,31 +64,41 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) combine_kernel(CombinePa
       const bool out_of_range = kChecked && r >= p.y_rows;
       if (out_of_range) atomicCAS(p.error_word, MOE_OK, MOE_ECORRUPT);
       bad |= r < 0 || out_of_range;
-      if (r >= 0 && !out_of_range) v[k] = ptx::ld_stream_v4(p.y + static_cast<int64_t>(r) * row_bytes + c * 16);
+      if (r >= 0 && !out_of_range) {
+#pragma unroll
+        for (int i = 0; i < CPT; ++i)
+          v[i][k] = ptx::ld_stream_v4(p.y + static_cast<int64_t>(r) * row_bytes + (c0 + i * CT) * 16);
+      }
     }
   }
-  if (bad) return;  // routing error reported by route_count: leave out[t] untouched
+  if (bad) return;  // routing error reported by the routing kernel: leave out[t] untouched
 
-  float a[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) a[j] = 0.0f;
+  float wk[KMAX];
   const float* wt = p.w + t * K;
 #pragma unroll
-  for (int k = 0; k < KMAX; ++k) {
-    if (k < K) {
-      const float w = __ldg(wt + k);
-      fma_word(v[k].x, w, a[0], a[1]);
-      fma_word(v[k].y, w, a[2], a[3]);
-      fma_word(v[k].z, w, a[4], a[5]);
-      fma_word(v[k].w, w, a[6], a[7]);
+  for (int k = 0; k < KMAX; ++k)
+    if (k < K) wk[k] = __ldg(wt + k);
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) {
+    float a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (k < K) {
+        fma_word(v[i][k].x, wk[k], a[0], a[1]);
+        fma_word(v[i][k].y, wk[k], a[2], a[3]);
+        fma_word(v[i][k].z, wk[k], a[4], a[5]);
+        fma_word(v[i][k].w, wk[k], a[6], a[7]);
+      }
     }
+    uint4 o;
+    o.x = pack_bf16x2(a[0], a[1]);
+    o.y = pack_bf16x2(a[2], a[3]);
+    o.z = pack_bf16x2(a[4], a[5]);
+    o.w = pack_bf16x2(a[6], a[7]);
+    ptx::st_v4(p.out + t * row_bytes + (c0 + i * CT) * 16, o);
   }
-  uint4 o;
-  o.x = pack_bf16x2(a[0], a[1]);
-  o.y = pack_bf16x2(a[2], a[3]);
-  o.z = pack_bf16x2(a[4], a[5]);
-  o.w = pack_bf16x2(a[6], a[7]);
-  ptx::st_v4(p.out + t * row_bytes + c * 16, o);
 }
 
 // ---- bulk variant: a producer warp gathers with the TMA engine ---------------
@@ -549,11 +561,19 @@ cudaError_t launch_bulk_k(const CombineParams& p, const CombineLaunch& l, cudaSt
 template <int KMAX>
 cudaError_t launch_k(const CombineParams& p, bool pdl, cudaStream_t stream) {
   constexpr int MIN_BLOCKS = KMAX >= 16 ? 2 : (KMAX >= 8 ? 3 : 4);
-  const long long threads = static_cast<long long>(p.T) * (p.H >> 3);
+  // K <= 2: four chunks per thread when the row splits evenly (more loads in
+  // flight per thread; measured on GB300, see the design notes).
+  const int cpt = KMAX <= 2 && (p.H >> 3) % 4 == 0 ? 4 : 1;
+  const long long threads = static_cast<long long>(p.T) * ((p.H >> 3) / cpt);
   const long long grid = (threads + kThreads - 1) / kThreads;
   if (grid == 0) return cudaSuccess;
   if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  return launch_kernel(combine_kernel<KMAX, MIN_BLOCKS>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0,
+  if constexpr (KMAX <= 2) {
+    if (cpt == 4)
+      return launch_kernel(combine_kernel<KMAX, MIN_BLOCKS, 4>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0,
+                           stream, pdl, p);
+  }
+  return launch_kernel(combine_kernel<KMAX, MIN_BLOCKS, 1>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0,
                        stream, pdl, p);
 }
 
