@@ -90,6 +90,10 @@ def _load() -> ctypes.CDLL:
         lib.oracle_quantize_fp8.restype = ctypes.c_int
         lib.oracle_float_to_e4m3.argtypes = [ctypes.c_float]
         lib.oracle_float_to_e4m3.restype = ctypes.c_uint8
+        lib.oracle_dispatch_dense.argtypes = [i32, i32, i32, i32, i32, p, p, i64, p, p, p, p]
+        lib.oracle_dispatch_dense.restype = ctypes.c_int
+        lib.oracle_combine_dense.argtypes = [i32, i32, i32, i32, p, i64, p, p, p, i64, p, p, p]
+        lib.oracle_combine_dense.restype = ctypes.c_int
         lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_double.restype = ctypes.c_double
         _lib = lib
@@ -280,6 +284,48 @@ def combine_two_level(y: np.ndarray, topk_idx: np.ndarray, topk_w: np.ndarray, s
     L = E // N
     ranks = np.array([len(set((idx[t] // L).tolist())) for t in range(T)], np.int32)
     return out, part, ranks
+
+
+def dispatch_dense(x: np.ndarray, topk_idx: np.ndarray, E: int, N: int, cap: int):
+    """Dispatch through a dense padded all-to-all (see ``oracle_dispatch_dense``):
+    (send_buf uint16 [N*N*cap, H], recv_buf uint16 [N*N*cap, H], expert_x
+    uint16 [T*K, H], send_pos int32 [T, K]).  Both buffers start as zeros,
+    so their padding rows are zero."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, H = x.shape
+    K = idx.shape[1]
+    send = np.zeros((N * N * cap, H), np.uint16)
+    recv = np.zeros((N * N * cap, H), np.uint16)
+    ex = np.zeros((T * K, H), np.uint16)
+    pos = np.zeros((T, K), np.int32)
+    rc = lib.oracle_dispatch_dense(T, H, K, E, N, _ptr(x), _ptr(idx), cap, _ptr(send), _ptr(recv), _ptr(ex),
+                                   _ptr(pos))
+    if rc != OK:
+        raise OracleError(rc, "oracle_dispatch_dense")
+    return send, recv, ex, pos
+
+
+def combine_dense(y: np.ndarray, topk_w: np.ndarray, slot_row: np.ndarray, send_pos: np.ndarray, N: int, cap: int):
+    """Combine through the dense padded all-to-all back (see
+    ``oracle_combine_dense``): (out uint16 [T, H], back_send, back_recv
+    uint16 [N*N*cap, H], zero padding)."""
+    lib = _load()
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    sr = np.ascontiguousarray(slot_row, dtype=np.int32)
+    sp = np.ascontiguousarray(send_pos, dtype=np.int32)
+    T, K = w.shape
+    H = y.shape[1]
+    bs = np.zeros((N * N * cap, H), np.uint16)
+    br = np.zeros((N * N * cap, H), np.uint16)
+    out = np.zeros((T, H), np.uint16)
+    rc = lib.oracle_combine_dense(T, H, K, N, _ptr(y), y.shape[0], _ptr(w), _ptr(sr), _ptr(sp), cap, _ptr(bs),
+                                  _ptr(br), _ptr(out))
+    if rc != OK:
+        raise OracleError(rc, "oracle_combine_dense")
+    return out, bs, br
 
 
 def float_to_bf16(f: float) -> int:

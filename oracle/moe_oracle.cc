@@ -67,6 +67,22 @@
 //    the receiving side then copies each send row to its grouped row.  The
 //    result equals the direct placement; only the path (one more copy of every
 //    row) differs.
+//  * Dense padded all-to-all ("Efficient and portable mixture-of-experts
+//    communication", Sharding and parallelism: torch's all_to_all needs
+//    padding, or a GPU-CPU synchronisation, because ranks send different
+//    numbers of tokens to each peer; Benchmarks: the dense all-to-all
+//    primitives are bandwidth-bound and move an order of magnitude more data
+//    than the sparse kernels).  Read as: every (source rank s, destination
+//    rank r) chunk is a block of `cap` rows, cap fixed ahead of the layer (no
+//    count exchange), at least the most rows one source can send to one rank,
+//    T/N * min(K, E/N); source s fills block s*N+r with its (token, slot)
+//    pairs whose expert lives on r, in (expert, token) order, and leaves the
+//    rest of the block as padding; the exchange moves every block whole,
+//    padding included (block s*N+r of the send buffer becomes block r*N+s of
+//    the receive buffer); the receiver then moves the rows into the grouped
+//    layout, expert by expert and source rank by source rank.  Combine
+//    returns the expert outputs the same way in reverse and then takes the
+//    same float32 chain as the receiver-only combine.
 //
 // All bf16 values are raw 16-bit patterns.
 
@@ -449,5 +465,113 @@ uint16_t oracle_double_to_bf16(double v) { return double_to_bf16_rne(v); }
 float oracle_fmaf(float a, float b, float c) { return std::fmaf(a, b, c); }
 uint8_t oracle_float_to_e4m3(float f) { return float_to_e4m3_rne_sat(f); }
 double oracle_e4m3_to_double(uint8_t b) { return e4m3_to_double(b); }
+
+// Dense padded all-to-all dispatch (see the header).  cap = rows per
+// (source rank, destination rank) block.
+//   send_buf  bf16 [N*N*cap, H]: block s*N+r, rows [0, n(s,r)) = the rows
+//             source rank s sends to rank r; later rows (padding) untouched
+//   recv_buf  bf16 [N*N*cap, H]: block r*N+s = block s*N+r of send_buf, all
+//             cap rows
+//   expert_x  bf16 [T*K, H]: the grouped layout (as oracle_dispatch)
+//   send_pos  int32 [T*K]: the send row of pair t*K+k
+// Returns ORACLE_EINVAL when cap < T/N * min(K, E/N), besides the errors of
+// oracle_dispatch.
+int oracle_dispatch_dense(int32_t T, int32_t H, int32_t K, int32_t E, int32_t N, const uint16_t* x,
+                          const int32_t* topk_idx, int64_t cap, uint16_t* send_buf, uint16_t* recv_buf,
+                          uint16_t* expert_x, int32_t* send_pos) {
+  int rc = check_sizes(T, H, K, E, N);
+  if (rc) return rc;
+  const int32_t Tr = T / N;
+  const int32_t L = E / N;
+  if (cap < static_cast<int64_t>(Tr) * std::min(K, L) || cap < 1) return ORACLE_EINVAL;
+  if (T > 0 && (!x || !topk_idx || !send_buf || !recv_buf || !expert_x || !send_pos)) return ORACLE_EINVAL;
+  rc = check_routes(T, K, E, topk_idx);
+  if (rc) return rc;
+  // Senders: source s walks the experts of rank r in order, and for each its
+  // tokens in order.
+  for (int32_t s = 0; s < N; ++s) {
+    for (int32_t r = 0; r < N; ++r) {
+      const int64_t block = static_cast<int64_t>(s) * N + r;
+      int64_t j = 0;
+      for (int32_t e = r * L; e < (r + 1) * L; ++e) {
+        for (int32_t t = s * Tr; t < (s + 1) * Tr; ++t) {
+          for (int32_t k = 0; k < K; ++k) {
+            if (topk_idx[static_cast<int64_t>(t) * K + k] != e) continue;
+            const int64_t row = block * cap + j;
+            std::memcpy(send_buf + row * H, x + static_cast<int64_t>(t) * H, sizeof(uint16_t) * H);
+            send_pos[static_cast<int64_t>(t) * K + k] = static_cast<int32_t>(row);
+            ++j;
+          }
+        }
+      }
+    }
+  }
+  // The exchange: every block whole, padding included.
+  for (int32_t s = 0; s < N; ++s)
+    for (int32_t r = 0; r < N; ++r)
+      std::memcpy(recv_buf + (static_cast<int64_t>(r) * N + s) * cap * H,
+                  send_buf + (static_cast<int64_t>(s) * N + r) * cap * H, sizeof(uint16_t) * cap * H);
+  // Receivers: rank r's rows, expert by expert, source rank by source rank.
+  int64_t row = 0;
+  for (int32_t r = 0; r < N; ++r) {
+    std::vector<int64_t> next(N, 0);  // next unread row of block r*N+s
+    for (int32_t e = r * L; e < (r + 1) * L; ++e) {
+      for (int32_t s = 0; s < N; ++s) {
+        // The block's rows of expert e: those of source s's tokens that chose e.
+        int64_t n_e = 0;
+        for (int32_t t = s * Tr; t < (s + 1) * Tr; ++t)
+          for (int32_t k = 0; k < K; ++k) n_e += topk_idx[static_cast<int64_t>(t) * K + k] == e;
+        for (int64_t i = 0; i < n_e; ++i, ++row) {
+          const int64_t src = (static_cast<int64_t>(r) * N + s) * cap + next[s] + i;
+          std::memcpy(expert_x + row * H, recv_buf + src * H, sizeof(uint16_t) * H);
+        }
+        next[s] += n_e;
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+// Dense padded all-to-all combine: the expert outputs y (grouped layout) go
+// back to their source ranks through padded blocks, then the receiver-only
+// float32 chain.
+//   slot_row   int32 [T*K] grouped row of each pair (from oracle_dispatch)
+//   send_pos   int32 [T*K] the dispatch's send row of each pair
+//   back_send  bf16 [N*N*cap, H]: block r*N+s, row j = the output for the
+//              pair that went to row j of the dispatch's block s*N+r (padding
+//              untouched)
+//   back_recv  bf16 [N*N*cap, H]: block s*N+r = block r*N+s of back_send
+//   out[t, h]  = bf16_rne( fma chain over k of w[t,k] * back_recv[send_pos[t*K+k], h] from +0.0f )
+int oracle_combine_dense(int32_t T, int32_t H, int32_t K, int32_t N, const uint16_t* y, int64_t y_rows,
+                         const float* topk_w, const int32_t* slot_row, const int32_t* send_pos, int64_t cap,
+                         uint16_t* back_send, uint16_t* back_recv, uint16_t* out) {
+  if (T < 0 || H < 1 || K < 1 || N < 1 || cap < 1) return ORACLE_EINVAL;
+  const int64_t blocks = static_cast<int64_t>(N) * N;
+  for (int64_t p = 0; p < static_cast<int64_t>(T) * K; ++p) {
+    if (slot_row[p] < 0 || slot_row[p] >= y_rows) return ORACLE_EINVAL;
+    if (send_pos[p] < 0 || send_pos[p] >= blocks * cap) return ORACLE_EINVAL;
+  }
+  // Each expert rank r sends back the outputs of the rows it received from s.
+  for (int64_t p = 0; p < static_cast<int64_t>(T) * K; ++p) {
+    const int64_t sr = send_pos[p] / cap, j = send_pos[p] % cap;  // block s*N+r, row j
+    const int64_t s = sr / N, r = sr % N;
+    std::memcpy(back_send + ((r * N + s) * cap + j) * H, y + static_cast<int64_t>(slot_row[p]) * H,
+                sizeof(uint16_t) * H);
+  }
+  for (int64_t s = 0; s < N; ++s)
+    for (int64_t r = 0; r < N; ++r)
+      std::memcpy(back_recv + (s * N + r) * cap * H, back_send + (r * N + s) * cap * H, sizeof(uint16_t) * cap * H);
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t h = 0; h < H; ++h) {
+      float acc = 0.0f;
+      for (int32_t k = 0; k < K; ++k) {
+        const int64_t row = send_pos[t * K + k];
+        acc = std::fmaf(topk_w[t * K + k], bf16_to_float(back_recv[row * H + h]), acc);
+      }
+      out[t * H + h] = float_to_bf16_rne(acc);
+    }
+  }
+  return ORACLE_OK;
+}
 
 }  // extern "C"
