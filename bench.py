@@ -60,14 +60,17 @@ def parse():
     return ap.parse_args()
 
 
-def algorithmic_bytes(w, payload="bf16", partial_rows=None, staged=False):
+def algorithmic_bytes(w, payload="bf16", partial_rows=None, staged=False, dense_cap=None):
     """Bytes a layer must move at minimum (see the design notes):
     dispatch reads x and writes T*K rows (bf16, or E4M3 bytes plus one float32
     scale per 128 elements); combine reads T*K bf16 rows and writes T rows;
     plus the routing metadata.  The two-level combine (partial_rows = the
     number of (token, rank) partials) also writes and reads back its partial
     rows.  The two-stage dispatch (staged) also writes every dispatched row
-    to its send buffer and reads it back."""
+    to its send buffer and reads it back.  The dense padded all-to-all
+    (dense_cap = rows per block) writes every dispatched row to its block,
+    moves all N*N*dense_cap block rows (read and write) each way, and moves
+    every dispatched row between its block and its grouped row each way."""
     T, H, K, E, N = w.T, w.H, w.K, w.E, w.N
     row = H * 2
     pairs = T * K
@@ -81,6 +84,12 @@ def algorithmic_bytes(w, payload="bf16", partial_rows=None, staged=False):
         dispatch_meta += 4 * pairs * 4
     combine = pairs * row + T * row
     combine_meta = pairs * 4 + pairs * 4
+    if dense_cap is not None:
+        block_rows = N * N * dense_cap
+        dispatch += 2 * block_rows * row + 2 * pairs * row
+        dispatch_meta += 2 * pairs * 4 + 2 * pairs * 4
+        combine += 2 * pairs * row + 2 * block_rows * row
+        combine_meta += 2 * pairs * 4
     if partial_rows is not None:
         combine += 2 * partial_rows * row
         combine_meta += pairs * 4 + (N + 1) * 4
@@ -605,10 +614,11 @@ def run_gpu(args):
 
 # The other workloads of the benchmark, timed in the same run with the
 # headline's method (two rotating buffer sets, one pair of CUDA events around
-# K layers); the DeepSeek-sized layer also with the fp8 dispatch payload.
+# K layers); the DeepSeek-sized layer also with the fp8 dispatch payload and
+# through the dense padded all-to-all (the pages' comparison system).
 # Steps per workload: at least ~20 ms of timed layers.
 EXTRA_WORKLOADS = [("tiny", "bf16", 4000), ("mixtral", "bf16", 1000), ("kimi", "bf16", 60), ("worst", "bf16", 120),
-                   ("deepseek", "fp8", 300)]
+                   ("deepseek", "fp8", 300), ("deepseek", "dense", 10)]
 
 
 def time_workload(name, payload, steps, dev, peak, warmup=10):
@@ -628,6 +638,8 @@ def time_workload(name, payload, steps, dev, peak, warmup=10):
     stream = torch.cuda.Stream(device=dev)
     g = torch.Generator(device=dev)
     g.manual_seed(w.seed)
+    layer = moe.MoELayer(T, H, K, E, N, device=dev)
+    cap = layer.dense_capacity() if payload == "dense" else None
     with torch.cuda.stream(stream):
         x0 = torch.from_numpy(li.x.view(np.int16)).to(dev)
         idx0 = torch.from_numpy(li.topk_idx).to(dev)
@@ -636,23 +648,30 @@ def time_workload(name, payload, steps, dev, peak, warmup=10):
         sets = []
         for _ in range(2):
             sets.append(dict(x=x0.clone(), idx=idx0.clone(), w=w0.clone(), y=y0.clone(),
-                             ex=torch.empty((T * K, H), dtype=torch.int16 if payload == "bf16" else torch.uint8,
+                             ex=torch.empty((T * K, H), dtype=torch.uint8 if payload == "fp8" else torch.int16,
                                             device=dev),
-                             xs=None if payload == "bf16" else torch.empty((T * K, H // 128), dtype=torch.float32,
-                                                                           device=dev),
+                             xs=None if payload != "fp8" else torch.empty((T * K, H // 128), dtype=torch.float32,
+                                                                          device=dev),
                              out=torch.empty((T, H), dtype=torch.int16, device=dev)))
         del x0, idx0, w0, y0
+        # Dense padded all-to-all: one pair of block buffers (scratch) for both sets.
+        blocks = None if cap is None else [torch.empty((N * N * cap, H), dtype=torch.int16, device=dev)
+                                           for _ in range(2)]
     torch.cuda.synchronize(dev)
-    layer = moe.MoELayer(T, H, K, E, N, device=dev)
 
     def step(s_):
         if payload == "bf16":
             layer.dispatch_send(s_["x"], s_["idx"], s_["ex"], stream)
+        elif payload == "dense":
+            layer.dispatch_send_dense(s_["x"], s_["idx"], cap, blocks[0], blocks[1], s_["ex"], stream)
         else:
             layer.dispatch_send_fp8(s_["x"], s_["idx"], s_["ex"], s_["xs"], stream)
         layer.dispatch_recv(stream)
         layer.combine_send(s_["y"], stream)
-        layer.combine_recv(s_["w"], s_["out"], stream)
+        if payload == "dense":
+            layer.combine_recv_dense(s_["w"], cap, blocks[0], blocks[1], s_["out"], stream)
+        else:
+            layer.combine_recv(s_["w"], s_["out"], stream)
 
     for i in range(warmup):
         step(sets[i % 2])
@@ -685,13 +704,18 @@ def time_workload(name, payload, steps, dev, peak, warmup=10):
     routing = {1: "route_count", 2: "route_local+route_finalize", 3: "route_cluster", 4: "route_pack (in the pack)",
                5: "route_pack (one CTA)"}[layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)]
     layer.close()
-    del sets, graph
+    del sets, graph, blocks
     torch.cuda.empty_cache()
-    ab = algorithmic_bytes(w, payload)["total"]
+    ab = algorithmic_bytes(w, "bf16" if payload == "dense" else payload, dense_cap=cap)["total"]
     best = min(us, us_graph)
-    return {"us": round(us, 2), "us_graph": round(us_graph, 2), "bytes": ab, "steps": steps,
-            "tbs": round(ab / best / 1e6, 3), "frac": round(ab / best / 1e3 / peak, 4),
-            "payload": payload, "routing": routing}
+    res = {"us": round(us, 2), "us_graph": round(us_graph, 2), "bytes": ab, "steps": steps,
+           "tbs": round(ab / best / 1e6, 3), "frac": round(ab / best / 1e3 / peak, 4),
+           "payload": "bf16" if payload == "dense" else payload, "routing": routing}
+    if cap is not None:
+        res.update({"exchange": "dense padded all-to-all", "capacity_rows_per_block": cap,
+                    "exchanged_rows_each_way": N * N * cap, "dispatched_rows": T * K,
+                    "exchange_to_sparse_rows": round(N * N * cap / (T * K), 2)})
+    return res
 
 
 def run_e2e(args, w, li, layer, stream, dev):

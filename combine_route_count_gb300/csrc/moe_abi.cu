@@ -211,6 +211,7 @@ struct moe_ctx {
   int combine_piece_bytes;  // 0 = automatic
   int combine_ctas_per_sm;  // 0 = as many as fit
   bool route_pack_ok;  // the one-kernel route+pack path can run this configuration
+  int64_t dense_cap;   // capacity of the last dispatch if it was moe_dispatch_send_dense, else 0
   int cluster_ctas;   // route_cluster shape for this configuration (0 = cannot be scheduled)
   int cluster_chunk;
   int cluster_warps;
@@ -872,6 +873,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     if (frc != MOE_OK) return frc;
     if (timed && cudaEventRecord(ctx->ev[1], s) != cudaSuccess) return MOE_ECUDA;
     ctx->pack_timed = timed;
+    ctx->dense_cap = 0;
     ctx->phase = kDispatched;
     return MOE_OK;
   }
@@ -888,6 +890,7 @@ MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_i
     if (timed && cudaEventRecord(ctx->ev[1], s) != cudaSuccess) return MOE_ECUDA;
     ctx->pack_timed = timed;
   }
+  ctx->dense_cap = 0;
   ctx->phase = kDispatched;
   return MOE_OK;
 }
@@ -939,6 +942,7 @@ MOE_API int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t*
     if (prc != MOE_OK) return prc;
   }
   ctx->pack_timed = false;  // the event-timed pack is that of moe_dispatch_send(_fp8) only
+  ctx->dense_cap = 0;
   ctx->phase = kDispatched;
   return MOE_OK;
 }
@@ -977,6 +981,7 @@ MOE_API int moe_dispatch_send_quantized(moe_ctx* ctx, const void* xq, const floa
     if (prc != MOE_OK) return prc;
   }
   ctx->pack_timed = false;
+  ctx->dense_cap = 0;
   ctx->phase = kDispatched;
   return MOE_OK;
 }
@@ -1051,6 +1056,7 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
     if (timed && cudaEventRecord(ctx->ev[1], s) != cudaSuccess) return MOE_ECUDA;
     ctx->pack_timed = timed;
   }
+  ctx->dense_cap = 0;
   ctx->phase = kDispatched;
   return MOE_OK;
 }
@@ -1087,6 +1093,69 @@ MOE_API int moe_combine_send(moe_ctx* ctx, const void* expert_y, int64_t expert_
   return MOE_OK;
 }
 
+namespace {
+
+// Enqueues the receiver-only combine of the context's variant:
+//   out[t] = bf16( fma chain over k of w[t,k] * y[table[t*K+k]] )
+// with table the grouped rows (slot_row) or, for the dense all-to-all, the
+// rows of the returned blocks.  MOE_OK, MOE_EINVAL or MOE_ECUDA.
+int enqueue_combine(moe_ctx* ctx, const void* y, int64_t y_rows, const int32_t* table, const float* topk_w, void* out,
+                    cudaStream_t cs) {
+  const moe_config& c = ctx->cfg;
+  moe::CombineParams cp = {};
+  cp.y = static_cast<const uint8_t*>(y);
+  cp.w = topk_w;
+  cp.slot_row = table;
+  cp.out = static_cast<uint8_t*>(out);
+  cp.T = c.num_tokens;
+  cp.K = c.top_k;
+  cp.H = c.hidden;
+  cp.y_rows = y_rows;
+  cp.error_word = ctx->error_word;
+  moe::CombineLaunch cl = {};
+  cl.pdl = ctx->pdl != 0;
+  cl.variant = combine_variant_of(ctx);
+  cl.grid = 0;
+  if (cl.variant == moe::kCombineBulk) {
+    // By default the CTAs take tokens in the strided order (the leftover
+    // tokens split evenly by pieces) with pieces of up to 4 KiB; measured on
+    // GB300 against a contiguous range with 2 KiB pieces: DeepSeek-sized
+    // layers 169.6 -> 167.6 us, Kimi-sized 700 -> 680 us, the worst case
+    // 352 -> 344 us.  (The strided order with 2 KiB pieces was slower.)
+    const bool strided = ctx->combine_order != 0;
+    cl.shape = moe::combine_bulk_shape(c.hidden, c.top_k, ctx->combine_stages, ctx->combine_piece_bytes,
+                                       ctx->max_smem_optin, strided ? 4096 : 2048);
+    cl.shape.hints = ctx->cache_hints;
+    cl.shape.drop_unit = ctx->test_drop_unit;
+    // Token queue (MOE_OPT_COMBINE_SCHEDULE; default on, not with the
+    // failure-injection hook).  Measured on GB300 (A/B, one box) against the
+    // strided static order: DeepSeek-sized layer 162.7 -> 160.4 us,
+    // Kimi-sized 659.2 -> 645.0, worst case 325.0 -> 318.1.  Claiming single
+    // (token, piece) units instead was slower than the static order
+    // (DeepSeek 164.0 -> 168.3, Kimi 661 -> 702): pieces of one token read
+    // by different CTAs at once lose the row locality of one CTA streaming
+    // a token's K rows piece after piece.
+    cl.shape.queue = ctx->combine_schedule != 0 && ctx->test_drop_unit < 0 ? 1 : 0;
+    if (cl.shape.queue && moe::combine_bulk_smem_bytes(cl.shape, c.top_k) > static_cast<size_t>(ctx->max_smem_optin))
+      cl.shape.queue = 0;
+    if (cl.shape.queue) cp.queue = ctx->queue + 1;
+    const size_t smem = moe::combine_bulk_smem_bytes(cl.shape, c.top_k);
+    if (smem > static_cast<size_t>(ctx->max_smem_optin)) return MOE_EINVAL;
+    const int fit = moe::smem_ctas_per_sm(smem);
+    int per_sm = ctx->combine_ctas_per_sm > 0 && ctx->combine_ctas_per_sm < fit ? ctx->combine_ctas_per_sm : fit;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t units = static_cast<int64_t>(c.num_tokens) * cl.shape.pieces;
+    int64_t grid = static_cast<int64_t>(grid_sms(ctx)) * per_sm;
+    if (grid > units) grid = units;
+    cl.grid = static_cast<int>(grid);
+    cl.shape.strided = strided ? 1 : 0;
+  }
+  if (moe::launch_combine(cp, cl, cs) != cudaSuccess) return MOE_ECUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
 MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void* stream) {
   NvtxRange nvtx_range("moe_combine_recv");
   if (!ctx) return MOE_EINVAL;
@@ -1094,62 +1163,155 @@ MOE_API int moe_combine_recv(moe_ctx* ctx, const float* topk_w, void* out, void*
   const moe_config& c = ctx->cfg;
   if (c.num_tokens > 0) {
     if (!topk_w || !out || !aligned(topk_w, 4) || !aligned(out, 16)) return MOE_EINVAL;
-    moe::CombineParams cp = {};
-    cp.y = static_cast<const uint8_t*>(ctx->expert_y);
-    cp.w = topk_w;
-    cp.slot_row = ctx->slot_row;
-    cp.out = static_cast<uint8_t*>(out);
-    cp.T = c.num_tokens;
-    cp.K = c.top_k;
-    cp.H = c.hidden;
-    cp.y_rows = ctx->expert_y_rows;
-    cp.error_word = ctx->error_word;
-    moe::CombineLaunch cl = {};
-    cl.pdl = ctx->pdl != 0;
-    cl.variant = combine_variant_of(ctx);
-    cl.grid = 0;
-    if (cl.variant == moe::kCombineBulk) {
-      // By default the CTAs take tokens in the strided order (the leftover
-      // tokens split evenly by pieces) with pieces of up to 4 KiB; measured on
-      // GB300 against a contiguous range with 2 KiB pieces: DeepSeek-sized
-      // layers 169.6 -> 167.6 us, Kimi-sized 700 -> 680 us, the worst case
-      // 352 -> 344 us.  (The strided order with 2 KiB pieces was slower.)
-      const bool strided = ctx->combine_order != 0;
-      cl.shape = moe::combine_bulk_shape(c.hidden, c.top_k, ctx->combine_stages, ctx->combine_piece_bytes,
-                                         ctx->max_smem_optin, strided ? 4096 : 2048);
-      cl.shape.hints = ctx->cache_hints;
-      cl.shape.drop_unit = ctx->test_drop_unit;
-      // Token queue (MOE_OPT_COMBINE_SCHEDULE; default on, not with the
-      // failure-injection hook).  Measured on GB300 (A/B, one box) against the
-      // strided static order: DeepSeek-sized layer 162.7 -> 160.4 us,
-      // Kimi-sized 659.2 -> 645.0, worst case 325.0 -> 318.1.  Claiming single
-      // (token, piece) units instead was slower than the static order
-      // (DeepSeek 164.0 -> 168.3, Kimi 661 -> 702): pieces of one token read
-      // by different CTAs at once lose the row locality of one CTA streaming
-      // a token's K rows piece after piece.
-      cl.shape.queue = ctx->combine_schedule != 0 && ctx->test_drop_unit < 0 ? 1 : 0;
-      if (cl.shape.queue &&
-          moe::combine_bulk_smem_bytes(cl.shape, c.top_k) > static_cast<size_t>(ctx->max_smem_optin))
-        cl.shape.queue = 0;
-      if (cl.shape.queue) cp.queue = ctx->queue + 1;
-      const size_t smem = moe::combine_bulk_smem_bytes(cl.shape, c.top_k);
-      if (smem > static_cast<size_t>(ctx->max_smem_optin)) return MOE_EINVAL;
-      const int fit = moe::smem_ctas_per_sm(smem);
-      int per_sm = ctx->combine_ctas_per_sm > 0 && ctx->combine_ctas_per_sm < fit ? ctx->combine_ctas_per_sm : fit;
-      if (per_sm < 1) per_sm = 1;
-      const int64_t units = static_cast<int64_t>(c.num_tokens) * cl.shape.pieces;
-      int64_t grid = static_cast<int64_t>(grid_sms(ctx)) * per_sm;
-      if (grid > units) grid = units;
-      cl.grid = static_cast<int>(grid);
-      cl.shape.strided = strided ? 1 : 0;
-    }
     const bool timed = ctx->kernel_events != 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (timed && cudaEventRecord(ctx->ev[2], cs) != cudaSuccess) return MOE_ECUDA;
-    if (moe::launch_combine(cp, cl, cs) != cudaSuccess) return MOE_ECUDA;
+    const int rc = enqueue_combine(ctx, ctx->expert_y, ctx->expert_y_rows, ctx->slot_row, topk_w, out, cs);
+    if (rc != MOE_OK) return rc;
     if (timed && cudaEventRecord(ctx->ev[3], cs) != cudaSuccess) return MOE_ECUDA;
     ctx->combine_timed = timed;
   }
+  ctx->expert_y = nullptr;
+  ctx->phase = kIdle;
+  return MOE_OK;
+}
+
+MOE_API int moe_dense_capacity(const moe_config* cfg, int64_t* rows) {
+  if (!rows) return MOE_EINVAL;
+  const int rc = moe_validate_config(cfg);
+  if (rc) return rc;
+  const int64_t Tr = cfg->num_tokens / cfg->num_ranks;
+  const int64_t L = cfg->num_experts / cfg->num_ranks;
+  const int64_t cap = Tr * (cfg->top_k < L ? cfg->top_k : L);
+  *rows = cap > 0 ? cap : 1;
+  return MOE_OK;
+}
+
+namespace {
+
+// Argument checks shared by the dense dispatch and combine: capacity at
+// least moe_dense_capacity, row indices of N*N*capacity within int32, both
+// block buffers that large and 16-byte aligned.
+int check_dense_args(const moe_ctx* ctx, int64_t capacity, const void* send_buf, const void* recv_buf,
+                     int64_t buf_rows) {
+  const moe_config& c = ctx->cfg;
+  int64_t need = 0;
+  if (moe_dense_capacity(&c, &need) != MOE_OK) return MOE_EINVAL;
+  if (capacity < need) return MOE_EINVAL;
+  const int64_t rows = static_cast<int64_t>(c.num_ranks) * c.num_ranks * capacity;
+  if (rows > INT32_MAX || buf_rows < rows) return MOE_EINVAL;
+  if (c.num_tokens > 0 && (!send_buf || !recv_buf || !aligned(send_buf, 16) || !aligned(recv_buf, 16)))
+    return MOE_EINVAL;
+  return MOE_OK;
+}
+
+}  // namespace
+
+MOE_API int moe_dispatch_send_dense(moe_ctx* ctx, const void* x, const int32_t* topk_idx, int64_t capacity,
+                                    void* send_buf, void* recv_buf, int64_t buf_rows, void* expert_x,
+                                    int64_t expert_x_rows, void* stream) {
+  NvtxRange nvtx_range("moe_dispatch_send_dense");
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->phase != kIdle) return MOE_ESTATE;
+  const moe_config& c = ctx->cfg;
+  const int64_t pairs = static_cast<int64_t>(c.num_tokens) * c.top_k;
+  const int arc = check_dense_args(ctx, capacity, send_buf, recv_buf, buf_rows);
+  if (arc != MOE_OK) return arc;
+  if (expert_x_rows < pairs) return MOE_EINVAL;
+  if (c.num_tokens > 0) {
+    if (!x || !topk_idx || !expert_x) return MOE_EINVAL;
+    if (!aligned(x, 16) || !aligned(expert_x, 16) || !aligned(topk_idx, 4)) return MOE_EINVAL;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rrc = enqueue_routing(ctx, topk_idx, s);
+  if (rrc != MOE_OK) return rrc;
+  if (c.num_tokens > 0) {
+    const int64_t row_bytes = static_cast<int64_t>(c.hidden) * 2;
+    moe::DenseLayoutParams lp = {};
+    lp.topk_idx = topk_idx;
+    lp.slot_row = ctx->slot_row;
+    lp.src_offsets = ctx->src_offsets;
+    lp.expert_offsets = ctx->expert_offsets;
+    lp.send_pos = ctx->send_pos;
+    lp.recv_pos = ctx->send_dest;
+    lp.T = c.num_tokens;
+    lp.K = c.top_k;
+    lp.E = c.num_experts;
+    lp.N = c.num_ranks;
+    lp.cap = capacity;
+    lp.error_word = ctx->error_word;
+    if (moe::launch_dense_layout(lp, ctx->num_sms, ctx->pdl != 0, s) != cudaSuccess) return MOE_ECUDA;
+    // Senders: every token row to its K block rows.
+    int prc = enqueue_pack(ctx, x, send_buf, buf_rows, ctx->send_pos, c.num_tokens, c.top_k, row_bytes,
+                           ctx->pdl != 0, true, -1, s);
+    if (prc != MOE_OK) return prc;
+    // The exchange: every block whole.
+    moe::DenseA2aParams ap = {};
+    ap.in = static_cast<const uint8_t*>(send_buf);
+    ap.out = static_cast<uint8_t*>(recv_buf);
+    ap.N = c.num_ranks;
+    ap.cap = capacity;
+    ap.row_bytes = row_bytes;
+    ap.error_word = ctx->error_word;
+    if (moe::launch_dense_a2a(ap, ctx->num_sms, ctx->pdl != 0, s) != cudaSuccess) return MOE_ECUDA;
+    // Receivers: block rows into the grouped rows.
+    moe::RowMoveParams mp = {};
+    mp.src = static_cast<const uint8_t*>(recv_buf);
+    mp.dst = static_cast<uint8_t*>(expert_x);
+    mp.src_row = ctx->send_dest;
+    mp.dst_row = ctx->slot_row;
+    mp.n = pairs;
+    mp.row_bytes = row_bytes;
+    mp.src_rows = buf_rows;
+    mp.dst_rows = expert_x_rows;
+    mp.error_word = ctx->error_word;
+    if (moe::launch_row_move(mp, ctx->num_sms, ctx->pdl != 0, s) != cudaSuccess) return MOE_ECUDA;
+  }
+  ctx->pack_timed = false;
+  ctx->phase = kDispatched;
+  ctx->dense_cap = capacity;
+  return MOE_OK;
+}
+
+MOE_API int moe_combine_recv_dense(moe_ctx* ctx, const float* topk_w, int64_t capacity, void* send_buf,
+                                   void* recv_buf, int64_t buf_rows, void* out, void* stream) {
+  NvtxRange nvtx_range("moe_combine_recv_dense");
+  if (!ctx) return MOE_EINVAL;
+  if (ctx->phase != kCombineSent || ctx->dense_cap == 0) return MOE_ESTATE;
+  if (capacity != ctx->dense_cap) return MOE_EINVAL;
+  const int arc = check_dense_args(ctx, capacity, send_buf, recv_buf, buf_rows);
+  if (arc != MOE_OK) return arc;
+  const moe_config& c = ctx->cfg;
+  if (c.num_tokens > 0) {
+    if (!topk_w || !out || !aligned(topk_w, 4) || !aligned(out, 16)) return MOE_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t row_bytes = static_cast<int64_t>(c.hidden) * 2;
+    // Each expert rank's outputs into the blocks they came in by.
+    moe::RowMoveParams mp = {};
+    mp.src = static_cast<const uint8_t*>(ctx->expert_y);
+    mp.dst = static_cast<uint8_t*>(send_buf);
+    mp.src_row = ctx->slot_row;
+    mp.dst_row = ctx->send_dest;
+    mp.n = static_cast<int64_t>(c.num_tokens) * c.top_k;
+    mp.row_bytes = row_bytes;
+    mp.src_rows = ctx->expert_y_rows;
+    mp.dst_rows = buf_rows;
+    mp.error_word = ctx->error_word;
+    if (moe::launch_row_move(mp, ctx->num_sms, ctx->pdl != 0, s) != cudaSuccess) return MOE_ECUDA;
+    // The exchange back: block r*N+s to block s*N+r, every block whole.
+    moe::DenseA2aParams ap = {};
+    ap.in = static_cast<const uint8_t*>(send_buf);
+    ap.out = static_cast<uint8_t*>(recv_buf);
+    ap.N = c.num_ranks;
+    ap.cap = capacity;
+    ap.row_bytes = row_bytes;
+    ap.error_word = ctx->error_word;
+    if (moe::launch_dense_a2a(ap, ctx->num_sms, ctx->pdl != 0, s) != cudaSuccess) return MOE_ECUDA;
+    // The receiver-only combine over the returned rows.
+    const int rc = enqueue_combine(ctx, recv_buf, buf_rows, ctx->send_pos, topk_w, out, s);
+    if (rc != MOE_OK) return rc;
+  }
+  ctx->combine_timed = false;
   ctx->expert_y = nullptr;
   ctx->phase = kIdle;
   return MOE_OK;

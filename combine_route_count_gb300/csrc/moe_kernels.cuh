@@ -225,6 +225,41 @@ struct StagedLayoutParams {
 };
 cudaError_t launch_staged_layout(const StagedLayoutParams& p, bool pdl, cudaStream_t stream);
 
+// Dense padded all-to-all (dense_a2a.cu): blocks of `cap` rows per
+// (source rank, destination rank) pair.
+struct DenseLayoutParams {
+  const int32_t* topk_idx;        // [T*K]
+  const int32_t* slot_row;        // [T*K] grouped row of each pair (-1 after a routing error)
+  const int32_t* src_offsets;     // [E*N]
+  const int32_t* expert_offsets;  // [E+1]
+  int32_t* send_pos;              // [T*K] row (s*N+r)*cap+j of the pair in the send buffer, -1 if none
+  int32_t* recv_pos;              // [T*K] row (r*N+s)*cap+j of the pair in the receive buffer, -1 if none
+  int32_t T, K, E, N;
+  int64_t cap;                    // rows per block, >= T/N * min(K, E/N)
+  int32_t* error_word;            // checked builds report MOE_ECORRUPT here
+};
+cudaError_t launch_dense_layout(const DenseLayoutParams& p, int sms, bool pdl, cudaStream_t stream);
+struct DenseA2aParams {
+  const uint8_t* in;     // [N*N*cap, row_bytes]
+  uint8_t* out;          // [N*N*cap, row_bytes]: block r*N+s = block s*N+r of in
+  int32_t N;
+  int64_t cap;
+  int64_t row_bytes;     // multiple of 16
+  const int32_t* error_word;  // MOE_EROUTE: nothing is copied (may be null)
+};
+cudaError_t launch_dense_a2a(const DenseA2aParams& p, int sms, bool pdl, cudaStream_t stream);
+struct RowMoveParams {
+  const uint8_t* src;
+  uint8_t* dst;
+  const int32_t* src_row;  // [n]
+  const int32_t* dst_row;  // [n]; an entry < 0 in either table skips the row
+  int64_t n;
+  int64_t row_bytes;       // multiple of 16
+  int64_t src_rows, dst_rows;  // buffer rows (checked builds verify the tables against them)
+  int32_t* error_word;
+};
+cudaError_t launch_row_move(const RowMoveParams& p, int sms, bool pdl, cudaStream_t stream);
+
 // Two-level combine (partial sums on the sending side, then on the receiver).
 struct TwoLevelParams {
   const uint8_t* y;             // [rows, H] bf16

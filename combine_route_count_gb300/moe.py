@@ -44,7 +44,8 @@ EXPORTS = ("moe_validate_config", "moe_workspace_bytes", "moe_recv_bound_rows", 
            "moe_ctx_destroy", "moe_ctx_set_option", "moe_ctx_get_option", "moe_dispatch_send", "moe_dispatch_recv",
            "moe_combine_send", "moe_combine_recv", "moe_get_error", "moe_strerror",
            "moe_dispatch_send_noalloc", "moe_dispatch_send_fp8", "moe_combine_recv_two_level", "moe_partial_rows",
-           "moe_dispatch_send_staged", "moe_kernel_times", "moe_dispatch_send_quantized")
+           "moe_dispatch_send_staged", "moe_kernel_times", "moe_dispatch_send_quantized",
+           "moe_dense_capacity", "moe_dispatch_send_dense", "moe_combine_recv_dense")
 
 
 class moe_config(ctypes.Structure):
@@ -91,6 +92,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_dispatch_send_fp8": ([P, P, P, P, P, I64, P], I),
         "moe_dispatch_send_quantized": ([P, P, P, P, P, P, I64, P], I),
         "moe_dispatch_send_staged": ([P, P, P, P, I64, P, I64, P], I),
+        "moe_dense_capacity": ([C, ctypes.POINTER(ctypes.c_int64)], I),
+        "moe_dispatch_send_dense": ([P, P, P, I64, P, P, I64, P, I64, P], I),
+        "moe_combine_recv_dense": ([P, P, I64, P, P, I64, P, P], I),
         "moe_dispatch_recv": ([P, ctypes.POINTER(moe_dispatch_layout), P], I),
         "moe_combine_send": ([P, P, I64, P], I),
         "moe_combine_recv": ([P, P, P, P], I),
@@ -199,6 +203,25 @@ def moe_dispatch_send_quantized(ctx: int, xq: Any, x_scales: Any, topk_idx: Any,
     _check(load_library().moe_dispatch_send_quantized(ctx, _ptr(xq), _ptr(x_scales), _ptr(topk_idx), _ptr(expert_xq),
                                                       _ptr(expert_scales), expert_rows, _stream(stream)),
            "moe_dispatch_send_quantized")
+
+
+def moe_dense_capacity(cfg: moe_config) -> int:
+    v = ctypes.c_int64(0)
+    _check(load_library().moe_dense_capacity(ctypes.byref(cfg), ctypes.byref(v)), "moe_dense_capacity")
+    return int(v.value)
+
+
+def moe_dispatch_send_dense(ctx: int, x: Any, topk_idx: Any, capacity: int, send_buf: Any, recv_buf: Any,
+                            buf_rows: int, expert_x: Any, expert_x_rows: int, stream: Any = None) -> None:
+    _check(load_library().moe_dispatch_send_dense(ctx, _ptr(x), _ptr(topk_idx), capacity, _ptr(send_buf),
+                                                  _ptr(recv_buf), buf_rows, _ptr(expert_x), expert_x_rows,
+                                                  _stream(stream)), "moe_dispatch_send_dense")
+
+
+def moe_combine_recv_dense(ctx: int, topk_w: Any, capacity: int, send_buf: Any, recv_buf: Any, buf_rows: int,
+                           out: Any, stream: Any = None) -> None:
+    _check(load_library().moe_combine_recv_dense(ctx, _ptr(topk_w), capacity, _ptr(send_buf), _ptr(recv_buf),
+                                                 buf_rows, _ptr(out), _stream(stream)), "moe_combine_recv_dense")
 
 
 def moe_dispatch_recv(ctx: int, stream: Any = None) -> moe_dispatch_layout:
@@ -381,6 +404,21 @@ class MoELayer:
         """Two-stage dispatch: send_buf bf16 [>= T*K, H] is caller scratch."""
         moe_dispatch_send_staged(self.ctx, x, topk_idx, send_buf, send_buf.shape[0], expert_x, expert_x.shape[0],
                                  stream)
+
+    def dense_capacity(self) -> int:
+        """Smallest block size of the dense padded all-to-all: T/N * min(K, E/N)."""
+        return moe_dense_capacity(self.cfg)
+
+    def dispatch_send_dense(self, x, topk_idx, capacity, send_buf, recv_buf, expert_x, stream: Any = None) -> None:
+        """Dispatch through the dense padded all-to-all: send_buf and recv_buf
+        bf16 [>= N*N*capacity, H] are caller scratch."""
+        moe_dispatch_send_dense(self.ctx, x, topk_idx, capacity, send_buf, recv_buf,
+                                min(send_buf.shape[0], recv_buf.shape[0]), expert_x, expert_x.shape[0], stream)
+
+    def combine_recv_dense(self, topk_w, capacity, send_buf, recv_buf, out, stream: Any = None) -> None:
+        """Combine through the dense padded all-to-all back (after dispatch_send_dense)."""
+        moe_combine_recv_dense(self.ctx, topk_w, capacity, send_buf, recv_buf,
+                               min(send_buf.shape[0], recv_buf.shape[0]), out, stream)
 
     def dispatch_send_quantized(self, xq, x_scales, topk_idx, expert_xq, expert_scales, stream: Any = None) -> None:
         """Pre-quantised payload: xq uint8 [T, H], x_scales float32 [T, H/128]."""

@@ -92,7 +92,8 @@ int moe_validate_config(const moe_config* cfg);
 
 /* Device workspace (bytes, a multiple of 256) that one context needs: counts,
  * offsets, slot_row, row_src, the error word, the send tables of
- * moe_dispatch_send_staged, the plan of moe_combine_recv_two_level and the
+ * moe_dispatch_send_staged and moe_dispatch_send_dense, the plan of
+ * moe_combine_recv_two_level and the
  * pack's and the combine's work-queue counters.  Allocate it 256-byte
  * aligned; its contents need no initialisation (every dispatch writes what it
  * later reads). */
@@ -191,12 +192,59 @@ int moe_dispatch_send_quantized(moe_ctx* ctx, const void* xq, const float* x_sca
 int moe_dispatch_send_staged(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* send_buf, int64_t send_rows,
                              void* expert_x, int64_t expert_x_rows, void* stream);
 
+/* ---- Dense padded all-to-all (the pages' comparison system) -----------------
+ * "Efficient and portable mixture-of-experts communication" (Sharding and
+ * parallelism): torch's all_to_all needs padding (or a GPU-CPU
+ * synchronisation) because ranks send different numbers of tokens to each
+ * peer; (Benchmarks) the dense all-to-all is bandwidth-bound and moves an
+ * order of magnitude more data than the sparse kernels.  These two calls run
+ * a layer that way on one GPU, for measuring that difference: every (source
+ * rank s, destination rank r) chunk is a block of `capacity` rows fixed before
+ * the layer, so no count is exchanged.
+ *
+ * Smallest valid capacity: the most rows one source rank can send to one
+ * rank, T/N * min(K, E/N) (at least 1).  MOE_EINVAL for an invalid config. */
+int moe_dense_capacity(const moe_config* cfg, int64_t* rows);
+
+/* Dispatch, send half, through the dense padded all-to-all.  Same routing and
+ * same grouped rows in expert_x as moe_dispatch_send; on the way:
+ *   send_buf block s*N+r (rows [(s*N+r)*capacity, +capacity)): source rank s's
+ *     rows for the experts of rank r, in (expert, token) order, then padding
+ *     (rows left as they were);
+ *   recv_buf block r*N+s = send_buf block s*N+r, all `capacity` rows
+ *     (padding included: the exchange moves N*N*capacity rows);
+ *   expert_x: the receivers' rows, grouped by expert.
+ *   capacity        >= moe_dense_capacity; N*N*capacity < 2^31
+ *   send_buf, recv_buf  device bf16 [buf_rows, H] each, caller-owned scratch,
+ *                   16-byte aligned, buf_rows >= N*N*capacity
+ *   x, topk_idx, expert_x, expert_x_rows  as for moe_dispatch_send
+ * Enqueues routing, a block-layout kernel (each pair's block rows), the bulk
+ * pack into send_buf, the exchange (dense_a2a) and a row copy into expert_x.
+ * After a routing error nothing is written to send_buf, recv_buf or expert_x.
+ * Errors and call order as for moe_dispatch_send; moe_combine_recv (grouped
+ * rows) or moe_combine_recv_dense may follow. */
+int moe_dispatch_send_dense(moe_ctx* ctx, const void* x, const int32_t* topk_idx, int64_t capacity, void* send_buf,
+                            void* recv_buf, int64_t buf_rows, void* expert_x, int64_t expert_x_rows, void* stream);
+
+/* Combine, receive half, through the dense padded all-to-all back: every
+ * expert rank returns its outputs (expert_y of moe_combine_send) in the
+ * blocks they came in by, the exchange moves block r*N+s of send_buf to block
+ * s*N+r of recv_buf whole, then the receiver-only combine of moe_combine_recv
+ * runs on the returned rows (same float32 chain, same bits).  Valid after
+ * moe_combine_send when the dispatch was moe_dispatch_send_dense with the same
+ * capacity (MOE_ESTATE otherwise; MOE_EINVAL for another capacity).
+ * send_buf and recv_buf as for moe_dispatch_send_dense (the dispatch's may be
+ * reused); out and topk_w as for moe_combine_recv. */
+int moe_combine_recv_dense(moe_ctx* ctx, const float* topk_w, int64_t capacity, void* send_buf, void* recv_buf,
+                           int64_t buf_rows, void* out, void* stream);
+
 /* Dispatch, receive half.  On one GPU the send half already placed every row
  * in the grouped layout (the shared-buffer case of "Efficient and portable
  * mixture-of-experts communication", Further improvements), so this enqueues
  * nothing: it fills `layout` with device pointers to the counts, offsets and
  * routing tables.  Valid after moe_dispatch_send, moe_dispatch_send_fp8,
- * moe_dispatch_send_quantized or moe_dispatch_send_staged. */
+ * moe_dispatch_send_quantized, moe_dispatch_send_staged or
+ * moe_dispatch_send_dense. */
 int moe_dispatch_recv(moe_ctx* ctx, moe_dispatch_layout* layout, void* stream);
 
 /* Combine, send half: registers the expert outputs, one row per dispatched
