@@ -1,10 +1,11 @@
 """Writes stay inside the caller's workspace, through the C ABI.
 
 The workspace holds every routing table (counts, offsets, slot_row, row_src,
-the error word), the send tables of the two-stage dispatch and the plan of
-the two-level combine.  Each test places it between canary bytes, drives one
-entry point after another on the same context (direct, fp8, already
-quantised and two-stage dispatch; receiver and two-level combine; a layer
+the error word), the send tables of the two-stage and the dense dispatch and
+the plan of the two-level combine.  Each test places it between canary
+bytes, drives one entry point after another on the same context (direct,
+fp8, already quantised, two-stage and dense dispatch; receiver, two-level
+and dense combine; a layer
 with a bad expert index, which makes every kernel take its error path) and
 checks that no canary byte changed and that the results still match the
 oracle where they are defined."""
@@ -103,6 +104,18 @@ def test_every_entry_point_stays_inside_the_workspace(moe, oracle_mod, shape):
     assert np.array_equal(out.cpu().numpy().view(np.uint16), ref2)
     assert guards_intact()
 
+    # dense padded all-to-all dispatch + combine (block tables in the workspace)
+    cap = layer.dense_capacity()
+    blocks = [torch.empty((N * N * cap, H), dtype=torch.int16, device="cuda") for _ in range(2)]
+    layer.dispatch_send_dense(x, idx, cap, blocks[0], blocks[1], ex)
+    layer.dispatch_recv()
+    layer.combine_send(y)
+    layer.combine_recv_dense(wt, cap, blocks[0], blocks[1], out)
+    assert layer.get_error() == 0
+    assert np.array_equal(ex.cpu().numpy().view(np.uint16), d.expert_x)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), out_ref)
+    assert guards_intact()
+
     # a bad expert index: every kernel takes its error path
     bad = li.topk_idx.copy()
     bad[T // 2, 0] = E
@@ -113,6 +126,11 @@ def test_every_entry_point_stays_inside_the_workspace(moe, oracle_mod, shape):
     layer.dispatch_recv()
     layer.combine_send(y)
     layer.combine_recv_two_level(wt, partial, out)
+    assert layer.get_error() == moe.MOE_EROUTE
+    layer.dispatch_send_dense(x, bad_d, cap, blocks[0], blocks[1], ex)
+    layer.dispatch_recv()
+    layer.combine_send(y)
+    layer.combine_recv_dense(wt, cap, blocks[0], blocks[1], out)
     assert layer.get_error() == moe.MOE_EROUTE
     assert guards_intact()
 
