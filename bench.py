@@ -61,7 +61,7 @@ def parse():
 
 
 def algorithmic_bytes(w, payload="bf16", partial_rows=None, staged=False, dense_cap=None):
-    """Bytes a layer must move at minimum (see the design notes):
+    """Bytes a layer must move at minimum:
     dispatch reads x and writes T*K rows (bf16, or E4M3 bytes plus one float32
     scale per 128 elements); combine reads T*K bf16 rows and writes T rows;
     plus the routing metadata.  The two-level combine (partial_rows = the

