@@ -472,7 +472,8 @@ def run_gpu(args):
     kernels = {
         "dispatch_send": {"us": round(disp_us, 2), "alone_us": round(disp_alone_us, 2), "bytes": ab["dispatch"],
                           "gbs": round(ab["dispatch"] / disp_us / 1e3, 1),
-                          "kernels": ["route_cluster", "dispatch_pack"] if args.dispatch == "direct"
+                          "kernels": (["route_pack"] if layer.get_option(moe.MOE_OPT_ROUTE_VARIANT) == 4
+                                      else ["route_cluster", "dispatch_pack"]) if args.dispatch == "direct"
                           else ["route_cluster", "staged_layout", "dispatch_pack (send rows)",
                                 "dispatch_pack (receive shuffle)"]},
         "combine_recv": {"us": round(comb_us, 2), "bytes": ab["combine"],
@@ -508,6 +509,8 @@ def run_gpu(args):
         comb_bytes = rows * H * 2 + T * H * 2 + rows * 8
         kernel_us = {"pack": statistics.mean(pk) * 1e3, "combine": statistics.mean(cb) * 1e3}
         kernels["dispatch_pack_kernel"] = {"us": round(kernel_us["pack"], 2), "bytes": pack_bytes,
+                                           "kernel": "route_pack" if layer.get_option(moe.MOE_OPT_ROUTE_VARIANT) == 4
+                                           else "dispatch_pack",
                                            "gbs": round(pack_bytes / kernel_us["pack"] / 1e3, 1),
                                            "timing": f"events around the kernel launch, {len(pk)} layers"}
         kernels["combine_kernel"] = {"us": round(kernel_us["combine"], 2), "bytes": comb_bytes,
