@@ -846,6 +846,10 @@ int enqueue_route_pack(moe_ctx* ctx, const void* x, const int32_t* topk_idx, voi
   rl.grid = static_cast<int>(grid);
   rl.copy_warps = warps;
   rl.stages = stages;
+  // Small rows, at most two per copy warp (a 64-token layer): through
+  // registers, no stages.
+  rl.vec = c.top_k <= 8 && rp.pieces == 1 &&
+           moe::route_pack_vec_ok(rp.row_bytes, (units + grid * warps - 1) / (grid * warps));
   rl.hints = ctx->cache_hints;
   rl.depth = ctx->pack_depth > 0 ? ctx->pack_depth : 2;
   rl.pdl = ctx->pdl != 0;

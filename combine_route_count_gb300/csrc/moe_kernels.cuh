@@ -116,6 +116,7 @@ struct RoutePackParams {
 struct RoutePackLaunch {
   int grid;        // CTAs (at most one per SM)
   int threads;     // block size: 256 or kRoutePackThreads (a multiple of 32, >= 32 * copy_warps)
+  bool vec;        // rows through registers instead of stages (route_pack_vec_ok); stages unused
   int copy_warps;  // warps per CTA that copy, each a virtual pack CTA (0..8; 0: routing only)
   int stages;      // shared-memory stages per copy warp (2..route_pack_max_stages)
   int hints;   // CacheHints
@@ -125,6 +126,8 @@ struct RoutePackLaunch {
 size_t route_pack_tables_bytes(int T, int E);
 size_t route_pack_smem_bytes(int T, int K, int E, int copy_warps, int stages, int piece_bytes);
 int route_pack_max_stages(int copy_warps);
+// Rows small and few enough per copy warp to go through registers.
+bool route_pack_vec_ok(int64_t row_bytes, int64_t units_per_warp);
 bool route_pack_eligible(int T, int K, int E);
 cudaError_t prepare_route_pack(int max_smem_bytes);  // one-time per-device attribute setup
 cudaError_t launch_route_pack(const RoutePackParams& p, const RoutePackLaunch& l, cudaStream_t stream);

@@ -134,7 +134,14 @@ __host__ __device__ inline size_t index_bytes(int T, int K) {
   return (static_cast<size_t>(T) * K * sizeof(int32_t) + 15) / 16 * 16;
 }
 
-template <int KMAX>
+// VEC (small rows, at most kVecUnits units of at most kVecChunks*512 bytes
+// per copy warp): the copy warps hold their rows in registers, loaded with
+// 16-byte loads while the tables are built, and store them with 16-byte
+// stores; no stages, no mbarriers, nothing to wait for before exiting.
+constexpr int kVecUnits = 2;
+constexpr int kVecChunks = 2;
+
+template <int KMAX, bool VEC>
 __global__ void __launch_bounds__(kRoutePackThreads, 1)
     route_pack_kernel(RoutePackParams p, int copy_warps, int stages, int hints, int depth) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -161,7 +168,7 @@ __global__ void __launch_bounds__(kRoutePackThreads, 1)
   const int64_t step = static_cast<int64_t>(gridDim.x) * copy_warps;
   const int64_t mine = copier && units > first ? (units - first + step - 1) / step : 0;
 
-  if (copier && lane == 0) {
+  if (!VEC && copier && lane == 0) {
     for (int s = 0; s < stages; ++s) ptx::mbar_init(&bars[s], 1);
     ptx::mbar_fence_init();
   }
@@ -212,9 +219,24 @@ __global__ void __launch_bounds__(kRoutePackThreads, 1)
                     p.x + t * p.row_bytes + static_cast<int64_t>(j) * p.piece_bytes, bytes, &bars[s]);
   };
   // Each copy warp's first token rows travel while the tables are built;
-  // its later rows go to L2.
-  const int64_t prologue = mine < stages ? mine : stages;
-  if (copier) {
+  // its later rows go to L2.  (VEC: all its rows, into registers.)
+  const int64_t prologue = VEC ? 0 : (mine < stages ? mine : stages);
+  const int64_t row_chunks = p.row_bytes >> 4;
+  uint4 vrow[VEC ? kVecUnits : 1][VEC ? kVecChunks : 1];
+  if (VEC && copier) {
+#pragma unroll
+    for (int u = 0; u < (VEC ? kVecUnits : 1); ++u) {
+      if (u < mine) {
+        const int64_t t = first + u * step;  // whole rows: unit = token
+#pragma unroll
+        for (int c = 0; c < (VEC ? kVecChunks : 1); ++c) {
+          const int64_t ch = static_cast<int64_t>(c) * 32 + lane;
+          if (ch < row_chunks) vrow[u][c] = ptx::ld_stream_v4(p.x + t * p.row_bytes + ch * 16);
+        }
+      }
+    }
+  }
+  if (!VEC && copier) {
     if (lane == 0)
       for (int64_t i = 0; i < prologue; ++i) issue_load(i);
     for (int64_t i = prologue + lane; i < mine; i += 32) {
@@ -364,6 +386,30 @@ __global__ void __launch_bounds__(kRoutePackThreads, 1)
     return;
   }
 
+  if (VEC) {
+#pragma unroll
+    for (int u = 0; u < (VEC ? kVecUnits : 1); ++u) {
+      if (u < mine) {
+        const int t = static_cast<int>(first + u * step);
+        const int my_row = lane < K ? row_of(t, sidx[t * K + lane]) : -1;
+        for (int k = 0; k < K; ++k) {
+          const int row = __shfl_sync(0xffffffffu, my_row, k);
+          if (kChecked && row >= p.dst_rows) {
+            if (lane == 0) atomicCAS(p.error_word, MOE_OK, MOE_ECORRUPT);
+            continue;
+          }
+          uint8_t* dst = p.expert_x + static_cast<int64_t>(row) * p.row_bytes;
+#pragma unroll
+          for (int c = 0; c < (VEC ? kVecChunks : 1); ++c) {
+            const int64_t ch = static_cast<int64_t>(c) * 32 + lane;
+            if (ch < row_chunks) ptx::st_v4(dst + ch * 16, vrow[u][c]);
+          }
+        }
+      }
+    }
+    return;
+  }
+
   // 5. the static bulk copy loop of this virtual CTA; destination rows one
   // unit ahead.
   auto dest_row = [&](int64_t unit_index) -> int {
@@ -446,10 +492,13 @@ int route_pack_max_stages(int copy_warps) {
 }
 
 cudaError_t prepare_route_pack(int max_smem_bytes) {
-  const void* kernels[] = {reinterpret_cast<const void*>(route_pack_kernel<2>),
-                           reinterpret_cast<const void*>(route_pack_kernel<4>),
-                           reinterpret_cast<const void*>(route_pack_kernel<8>),
-                           reinterpret_cast<const void*>(route_pack_kernel<16>)};
+  const void* kernels[] = {reinterpret_cast<const void*>(route_pack_kernel<2, false>),
+                           reinterpret_cast<const void*>(route_pack_kernel<4, false>),
+                           reinterpret_cast<const void*>(route_pack_kernel<8, false>),
+                           reinterpret_cast<const void*>(route_pack_kernel<16, false>),
+                           reinterpret_cast<const void*>(route_pack_kernel<2, true>),
+                           reinterpret_cast<const void*>(route_pack_kernel<4, true>),
+                           reinterpret_cast<const void*>(route_pack_kernel<8, true>)};
   for (const void* k : kernels) {
     const cudaError_t err = set_kernel_limits(k, static_cast<size_t>(max_smem_bytes));
     if (err != cudaSuccess) return err;
@@ -457,26 +506,31 @@ cudaError_t prepare_route_pack(int max_smem_bytes) {
   return cudaSuccess;
 }
 
+bool route_pack_vec_ok(int64_t row_bytes, int64_t units_per_warp) {
+  return row_bytes <= kVecChunks * 512 && units_per_warp <= kVecUnits;
+}
+
 cudaError_t launch_route_pack(const RoutePackParams& p, const RoutePackLaunch& l, cudaStream_t stream) {
+  const bool vec = l.vec && p.K <= 8;  // K > 8 keeps its rows in stages (registers would spill)
   const int maxst = route_pack_max_stages(l.copy_warps);
-  const int stages = l.stages < 2 ? 2 : (l.stages > maxst ? maxst : l.stages);
+  const int stages = vec ? 0 : (l.stages < 2 ? 2 : (l.stages > maxst ? maxst : l.stages));
   const size_t smem = route_pack_smem_bytes(p.T, p.K, p.E, l.copy_warps, stages, p.piece_bytes);
-  const int depth = clamp_depth(l.depth, stages);
+  const int depth = vec ? 1 : clamp_depth(l.depth, stages);
   const int threads = l.threads >= 32 * (l.copy_warps > 1 ? l.copy_warps : 1) && l.threads <= kRoutePackThreads
                           ? l.threads / 32 * 32
                           : kRoutePackThreads;
   const dim3 grid(l.grid), block(threads);
-  if (p.K <= 2)
-    return launch_kernel(route_pack_kernel<2>, grid, block, smem, stream, l.pdl, p, l.copy_warps, stages, l.hints,
-                         depth);
-  if (p.K <= 4)
-    return launch_kernel(route_pack_kernel<4>, grid, block, smem, stream, l.pdl, p, l.copy_warps, stages, l.hints,
-                         depth);
-  if (p.K <= 8)
-    return launch_kernel(route_pack_kernel<8>, grid, block, smem, stream, l.pdl, p, l.copy_warps, stages, l.hints,
-                         depth);
-  return launch_kernel(route_pack_kernel<16>, grid, block, smem, stream, l.pdl, p, l.copy_warps, stages, l.hints,
-                       depth);
+#define MOE_RP_LAUNCH(KM)                                                                                      \
+  return vec ? launch_kernel(route_pack_kernel<KM, true>, grid, block, smem, stream, l.pdl, p, l.copy_warps, \
+                               stages, l.hints, depth)                                                         \
+               : launch_kernel(route_pack_kernel<KM, false>, grid, block, smem, stream, l.pdl, p, l.copy_warps, \
+                               stages, l.hints, depth)
+  if (p.K <= 2) MOE_RP_LAUNCH(2);
+  if (p.K <= 4) MOE_RP_LAUNCH(4);
+  if (p.K <= 8) MOE_RP_LAUNCH(8);
+#undef MOE_RP_LAUNCH
+  return launch_kernel(route_pack_kernel<16, false>, grid, block, smem, stream, l.pdl, p, l.copy_warps, stages,
+                       l.hints, depth);
 }
 
 }  // namespace moe
