@@ -30,23 +30,26 @@
 //   3. one exclusive scan of the chunk totals in (expert, chunk) order:
 //      the expert offsets and every chunk's first row at once;
 //   4. the stable row of (t, k) with e = idx[t, k] is
-//        off[e] + pre[e][t/32] + popc(mask[e][t/32] & lanes below t%32),
+//        cpre[e][chunk of t] + pre[e][t/32] + popc(mask[e][t/32] & lanes below t%32),
 //      the same placement as route_count and route_cluster (by expert, then
 //      by token); the CTA writes slot_row and row_src of tokens b, b+G, ...;
 //      CTA 0 writes counts, offsets, per-(expert, source rank) and per-rank
 //      offsets and the status word;
 //   5. warps w < P run the bulk pack's static copy loop as virtual CTA
 //      v = b*P + w of G*P (units v, v+GP, ...), taking destination rows from
-//      the tables in shared memory.
+//      the tables in shared memory; or, when a copy warp has at most two
+//      small whole rows (VEC), it loads them into registers right after the
+//      dependency wait and stores them once the tables are built.
 //
 // The redundant routing costs each CTA a T*K*4-byte copy from L2 and
 // ~T*K/32 warp instructions; the host picks this kernel only when that is
 // small (see route_pack_eligible).  Reading the indices from shared memory
 // matters: with per-lane global loads the compiler may issue each word's
 // loads just before their use, and a Mixtral-sized layer spent ~15 us of
-// serialised round trips (queued behind the token rows) in step 1.  Every CTA reaches the same verdict on a
-// malformed routing, so after a routing error no CTA copies anything and
-// every slot_row entry becomes -1 (the combine then writes nothing).
+// serialised round trips (queued behind the token rows) in step 1.  Every
+// CTA reaches the same verdict on a malformed routing, so after a routing
+// error no CTA copies anything and every slot_row entry becomes -1 (the
+// combine then writes nothing).
 
 #include <cuda_runtime.h>
 
