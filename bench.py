@@ -469,11 +469,14 @@ def run_gpu(args):
     # Inside the layer the pack's tail overlaps the combine's start; the
     # dispatch phase's share of the layer is what the combine leaves.
     disp_us = max(us_layer * ws - comb_us, 1e-3)
+    fused = route_of(layer, moe, args.payload, args.dispatch) == 4
+    pack_name = "dispatch_pack" if args.payload == "bf16" else "dispatch_pack_fp8"
+    fused_name = "route_pack" if args.payload == "bf16" else "route_pack_fp8"
     kernels = {
         "dispatch_send": {"us": round(disp_us, 2), "alone_us": round(disp_alone_us, 2), "bytes": ab["dispatch"],
                           "gbs": round(ab["dispatch"] / disp_us / 1e3, 1),
-                          "kernels": (["route_pack"] if layer.get_option(moe.MOE_OPT_ROUTE_VARIANT) == 4
-                                      else ["route_cluster", "dispatch_pack"]) if args.dispatch == "direct"
+                          "kernels": ([fused_name] if fused else ["route_cluster", pack_name])
+                          if args.dispatch == "direct"
                           else ["route_cluster", "staged_layout", "dispatch_pack (send rows)",
                                 "dispatch_pack (receive shuffle)"]},
         "combine_recv": {"us": round(comb_us, 2), "bytes": ab["combine"],
@@ -509,8 +512,7 @@ def run_gpu(args):
         comb_bytes = rows * H * 2 + T * H * 2 + rows * 8
         kernel_us = {"pack": statistics.mean(pk) * 1e3, "combine": statistics.mean(cb) * 1e3}
         kernels["dispatch_pack_kernel"] = {"us": round(kernel_us["pack"], 2), "bytes": pack_bytes,
-                                           "kernel": "route_pack" if layer.get_option(moe.MOE_OPT_ROUTE_VARIANT) == 4
-                                           else "dispatch_pack",
+                                           "kernel": fused_name if fused else pack_name,
                                            "gbs": round(pack_bytes / kernel_us["pack"] / 1e3, 1),
                                            "timing": f"events around the kernel launch, {len(pk)} layers"}
         kernels["combine_kernel"] = {"us": round(kernel_us["combine"], 2), "bytes": comb_bytes,
@@ -521,7 +523,7 @@ def run_gpu(args):
             dom, dom_us, dom_bytes, dom_kernel = "combine", kernel_us["combine"], comb_bytes, "combine"
         else:
             dom, dom_us, dom_bytes = "dispatch_pack", kernel_us["pack"], pack_bytes
-            dom_kernel = "dispatch_pack" if args.payload == "bf16" else "dispatch_pack_fp8"
+            dom_kernel = fused_name if fused else pack_name
     elif comb_us >= disp_us:
         dom, dom_us, dom_bytes = "combine", comb_us, ab["combine"]
         dom_kernel = "combine" if args.combine == "receiver" else "combine_two_level"
@@ -701,10 +703,9 @@ def time_workload(name, payload, steps, dev, peak, warmup=10):
     status = layer.get_error(stream)
     if status != moe.MOE_OK:
         raise RuntimeError(f"device reported status {status} timing {name}")
-    v = layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)
-    if v == 4 and payload != "bf16":
-        v = 3 if layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS) > 0 else 2
-    routing = {1: "route_count", 2: "route_local+route_finalize", 3: "route_cluster", 4: "route_pack (in the pack)",
+    v = route_of(layer, moe, "bf16" if payload == "dense" else payload, "dense" if payload == "dense" else "direct")
+    routing = {1: "route_count", 2: "route_local+route_finalize", 3: "route_cluster",
+               4: "route_pack (in the pack)" if payload != "fp8" else "route_pack_fp8 (in the fp8 pack)",
                5: "route_pack (one CTA)"}[v]
     layer.close()
     del sets, graph, blocks
@@ -721,16 +722,29 @@ def time_workload(name, payload, steps, dev, peak, warmup=10):
     return res
 
 
-def routing_label(layer, moe, args):
-    """The routing kernels the timed dispatch runs.  The automatic choice
-    reported by the context is that of moe_dispatch_send; the other dispatch
-    forms never route inside the pack."""
+def route_of(layer, moe, payload, dispatch="direct"):
+    """The routing path of the timed dispatch (the MOE_OPT_ROUTE_VARIANT
+    numbering): the context reports moe_dispatch_send's and
+    moe_dispatch_send_fp8's; the other dispatch forms never route inside the
+    pack."""
+    if dispatch == "direct" and payload == "bf16":
+        return layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)
+    if dispatch == "direct" and payload == "fp8":
+        return layer.get_option(moe.MOE_OPT_ROUTE_VARIANT_FP8)
     v = layer.get_option(moe.MOE_OPT_ROUTE_VARIANT)
-    if v == 4 and (args.payload != "bf16" or args.dispatch != "direct"):
+    if v == 4:
         v = 3 if layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS) > 0 else 2
+    return v
+
+
+def routing_label(layer, moe, args):
+    """The routing kernels the timed dispatch runs."""
+    v = route_of(layer, moe, args.payload, args.dispatch)
     return {1: "route_count (1 block)", 2: "route_local+route_finalize",
             3: f"route_cluster ({layer.get_option(moe.MOE_OPT_ROUTE_CLUSTER_CTAS)} CTAs)",
-            4: "route_pack (routing inside the pack kernel)", 5: "route_pack (routing alone in one CTA)"}[v]
+            4: "route_pack (routing inside the pack kernel)" if args.payload != "fp8"
+            else "route_pack_fp8 (routing inside the fp8 pack kernel)",
+            5: "route_pack (routing alone in one CTA)"}[v]
 
 
 def run_e2e(args, w, li, layer, stream, dev):

@@ -19,7 +19,7 @@ LIB = os.path.join(PKG, "libmoe.so")
 # its buffer before use (MOE_ECORRUPT); a separate library and object folder.
 BUILD_CHECKED = os.path.join(PKG, "_build_checked")
 LIB_CHECKED = os.path.join(PKG, "libmoe_checked.so")
-SOURCES = ["route_count.cu", "route_split.cu", "route_cluster.cu", "route_pack.cu", "dispatch_pack.cu", "dispatch_fp8.cu", "dispatch_staged.cu", "dense_a2a.cu", "combine.cu", "combine_two_level.cu", "moe_abi.cu", "moe_noalloc.cu"]
+SOURCES = ["route_count.cu", "route_split.cu", "route_cluster.cu", "route_pack.cu", "route_pack_fp8.cu", "dispatch_pack.cu", "dispatch_fp8.cu", "dispatch_staged.cu", "dense_a2a.cu", "combine.cu", "combine_two_level.cu", "moe_abi.cu", "moe_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

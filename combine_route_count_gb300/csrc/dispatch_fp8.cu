@@ -4,31 +4,25 @@
 // dispatch kernel sends tokens together with their block scaling factors;
 // "Enabling trillion-parameter models on AWS EFA" (evaluation): block-scale
 // fp8 dispatch, bf16 combine.  Each token row is quantised once and written
-// to its K destination rows:
-//   blocks of 128 consecutive elements, scale = amax / 448 (1 for an all-zero
-//   block), inv = 1 / scale (both IEEE float32 divisions, once per block),
-//   q = E4M3(x * inv) rounded to nearest even, saturating;
+// to its K destination rows (block scales of 128 elements, fp8_quant.cuh):
 //   expert_xq[slot_row[t,k]] = q[t], expert_scales[slot_row[t,k]] = scales[t].
 //
 // CTA = 1 producer warp + 4 consumer warps; unit = one token row; each CTA
 // takes a contiguous range of tokens.  The producer bulk-loads rows into
 // shared-memory stages (the first ones before griddepcontrol.wait: rows do
-// not depend on routing).  Consumers: 8 lanes cover one 128-element block (16
-// elements each), reduce amax with shuffles, multiply by the block's inverse
-// scale, convert two at a time with cvt.rn.satfinite.e4m3x2.f32 and store 16
-// fp8 bytes per lane to
-// each of the K destination rows (coalesced); one lane per block stores the
-// scale.  Waits are bounded (2 s) and report MOE_ETIMEDOUT.
+// not depend on routing); the 128 consumer threads quantise each row
+// together.  Waits are bounded (2 s) and report MOE_ETIMEDOUT.
 
 #include <cuda_runtime.h>
 
 #include "moe_kernels.cuh"
+#include "fp8_quant.cuh"
 #include "ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kConsumers = 128;
+constexpr int kConsumers = fp8q::kRowThreads;
 constexpr int kMaxFp8Stages = 8;
 constexpr int kFp8BarBytes = 256;
 // Queue variant: mbarriers, stage_tok[8] and stage_rows[8][16] before the stages.
@@ -52,73 +46,6 @@ __device__ __forceinline__ bool wait_parity(uint64_t* bar, uint32_t parity) {
 
 __device__ __forceinline__ void arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ptx::smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(const void* p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(ptx::smem_addr(p)));
-  return v;
-}
-
-// Two floats to two E4M3 codes: `lo` in the low byte, `hi` in the high byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// Consumer warps (thread c0 = 0..127 of them): quantise the bf16 row in shared
-// memory and store its codes and block scales to the K destination rows; lane
-// k of every consumer warp holds destination row k in my_row.
-template <int KMAX>
-__device__ __forceinline__ void quantize_row(const PackFp8Params& p, const uint8_t* row, int my_row, int c0,
-                                             int chunks, int nblk) {
-  const int K = p.K, H = p.H;
-  // Warp-uniform trip count: every lane reaches the shuffles below; lanes
-  // past the end of the row work on zeros and store nothing.
-  for (int cb = 0; cb < chunks; cb += kConsumers) {
-    const int c = cb + c0;
-    const bool act = c < chunks;
-    const uint4 a = act ? lds128(row + c * 32) : make_uint4(0, 0, 0, 0);
-    const uint4 b = act ? lds128(row + c * 32 + 16) : make_uint4(0, 0, 0, 0);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    float f[16];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      f[2 * j] = __uint_as_float(w[j] << 16);
-      f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    // The 8 lanes of one 128-element block are 8 consecutive lanes.
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-    const float inv = __fdiv_rn(1.0f, scale);
-    uint4 out;
-    uint32_t* o = &out.x;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t lo = e4m3x2(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
-      const uint32_t hi = e4m3x2(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
-      o[j] = lo | (hi << 16);
-    }
-    const int blk = c >> 3;
-#pragma unroll
-    for (int k = 0; k < KMAX; ++k) {
-      if (k < K) {
-        const int64_t dst = static_cast<int64_t>(__shfl_sync(0xffffffffu, my_row, k));
-        if (act) {
-          ptx::st_v4(p.expert_xq + dst * H + static_cast<int64_t>(c) * 16, out);
-          if ((c & 7) == 0) p.expert_scales[dst * nblk + blk] = scale;
-        }
-      }
-    }
-  }
 }
 
 // STRIDED: CTA b takes tokens b, b+G, b+2G, ... (G CTAs), so that the CTAs
@@ -199,7 +126,7 @@ __global__ void __launch_bounds__(32 + kConsumers, KMAX <= 4 ? 8 : 1) dispatch_p
     const bool skip = __any_sync(0xffffffffu, lane < K && my_row < 0);
     const uint8_t* row = stage_buf + s * row_bytes;
     if (!skip) {
-      quantize_row<KMAX>(p, row, my_row, c0, chunks, nblk);
+      fp8q::quantize_row<KMAX>(p, row, my_row, c0, chunks, nblk);
     }
     __syncwarp();
     if (lane == 0) arrive(&empty[s]);
@@ -316,7 +243,7 @@ __global__ void __launch_bounds__(32 + kConsumers, KMAX <= 4 ? 8 : 1)
     }
     // Routing error: slot_row is -1 everywhere, nothing is written.
     if (!__any_sync(0xffffffffu, lane < K && my_row < 0))
-      quantize_row<KMAX>(p, stage_buf + s * row_bytes, my_row, c0, chunks, nblk);
+      fp8q::quantize_row<KMAX>(p, stage_buf + s * row_bytes, my_row, c0, chunks, nblk);
     __syncwarp();
     if (lane == 0) arrive(&empty[s]);
   }

@@ -211,6 +211,7 @@ struct moe_ctx {
   int combine_piece_bytes;  // 0 = automatic
   int combine_ctas_per_sm;  // 0 = as many as fit
   bool route_pack_ok;  // the one-kernel route+pack path can run this configuration
+  bool route_pack_fp8_ok;  // ... and its fp8 form (moe_dispatch_send_fp8)
   int64_t dense_cap;   // capacity of the last dispatch if it was moe_dispatch_send_dense, else 0
   int cluster_ctas;   // route_cluster shape for this configuration (0 = cannot be scheduled)
   int cluster_chunk;
@@ -267,6 +268,7 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
   if (moe::route_local_smem_bytes(cfg->num_experts) > static_cast<size_t>(optin)) return MOE_EINVAL;
   if (moe::prepare_pack(optin) != cudaSuccess) return MOE_ECUDA;
   if (moe::prepare_route_pack(optin) != cudaSuccess) return MOE_ECUDA;
+  if (moe::prepare_route_pack_fp8(optin) != cudaSuccess) return MOE_ECUDA;
 
   moe_ctx* c = new (std::nothrow) moe_ctx;
   if (!c) return MOE_EINVAL;
@@ -321,6 +323,11 @@ MOE_API int moe_ctx_create(const moe_config* cfg, void* workspace, size_t worksp
                        moe::route_pack_smem_bytes(cfg->num_tokens, cfg->top_k, cfg->num_experts, 1, 2,
                                                   static_cast<int>(piece)) <=
                            static_cast<size_t>(optin);
+    // The fp8 form: two whole bf16 rows of one group next to the tables.
+    c->route_pack_fp8_ok = moe::route_pack_eligible(cfg->num_tokens, cfg->top_k, cfg->num_experts) &&
+                           cfg->hidden % MOE_FP8_BLOCK == 0 &&
+                           moe::route_pack_fp8_smem_bytes(cfg->num_tokens, cfg->top_k, cfg->num_experts,
+                                                          cfg->hidden, 1, 2) <= static_cast<size_t>(optin);
   }
   // Largest cluster of route_cluster CTAs this device can schedule for this
   // configuration (16, else 8, 4, 2, 1), or none.
@@ -382,6 +389,15 @@ bool dispatch_uses_route_pack(const moe_ctx* c) {
   if (!c->route_pack_ok) return false;
   if (c->route_variant == 4) return true;
   return c->route_variant == 0 && c->pack_variant == moe::kPackBulk && c->pack_schedule != 1;
+}
+
+// Whether moe_dispatch_send_fp8 routes and quantises in one kernel
+// (route_pack_fp8): forced by MOE_OPT_ROUTE_VARIANT 4, or automatic for the
+// same small layers, in the strided token order and without the token queue.
+bool dispatch_fp8_uses_route_pack(const moe_ctx* c) {
+  if (!c->route_pack_fp8_ok) return false;
+  if (c->route_variant == 4) return true;
+  return c->route_variant == 0 && c->fp8_order == 1 && c->pack_schedule != 1;
 }
 
 }  // namespace
@@ -527,6 +543,12 @@ MOE_API int moe_ctx_get_option(const moe_ctx* ctx, int option, int64_t* value) {
     case MOE_OPT_ROUTE_CLUSTER_CTAS:
       *value = ctx->cluster_ctas;
       return MOE_OK;
+    case MOE_OPT_ROUTE_VARIANT_FP8:
+      *value = dispatch_fp8_uses_route_pack(ctx)                                ? 4
+               : ctx->route_variant != 0 && ctx->route_variant != 4           ? ctx->route_variant
+               : ctx->cluster_ctas > 0                                          ? 3
+                                                                                : 2;
+      return MOE_OK;
     case MOE_OPT_COMBINE_VARIANT:
       *value = combine_variant_of(ctx);
       return MOE_OK;
@@ -625,8 +647,9 @@ int enqueue_routing(moe_ctx* ctx, const int32_t* topk_idx, cudaStream_t s) {
   int vec = 1;
   if (c.top_k % 4 == 0 && aligned(topk_idx, 16)) vec = 4;
   else if (c.top_k % 2 == 0 && aligned(topk_idx, 8)) vec = 2;
-  // Variant 4 (one-kernel route+pack) exists only for moe_dispatch_send;
-  // every other dispatch form routes as in the automatic choice.
+  // Variant 4 (one-kernel route+pack) exists only for moe_dispatch_send and
+  // moe_dispatch_send_fp8; every other dispatch form routes as in the
+  // automatic choice.
   const bool use_cluster =
       (ctx->route_variant == 0 || ctx->route_variant == 3 || ctx->route_variant == 4) && ctx->cluster_ctas > 0;
   if (ctx->route_variant == 1) {
@@ -857,6 +880,67 @@ int enqueue_route_pack(moe_ctx* ctx, const void* x, const int32_t* topk_idx, voi
   return MOE_OK;
 }
 
+// Enqueues route_pack_fp8: routing and the fp8 pack of x into expert_xq /
+// expert_scales in one kernel (moe_dispatch_send_fp8 of a small layer), one
+// CTA per SM.  Groups of 128 threads per CTA (MOE_OPT_PACK_CTAS_PER_SM, else
+// 2 for layers of at most 32 words of 32 tokens, whose routing is fastest
+// with 8 warps as for route_pack, and 7 otherwise), whole-row stages per
+// group (MOE_OPT_PACK_STAGES, else as many as fit next to the routing
+// tables); groups drop until two stages fit.  Measured on GB300 (A/B, one
+// box), Mixtral-sized fp8 layer with 2..8 groups: 42.8, 36.6, 34.2, 33.5,
+// 32.9, 31.8 (7 groups of 3 stages; 31.8 with 2 stages too) and 33.1 us (8
+// groups of 2 stages), against 33.6 us for route_cluster + the fp8 pack; the
+// 64-token layer in a graph: 6.05 us with 1 or 2 groups, 6.6 with 4, against
+// 8.6 us.  MOE_OK, MOE_EINVAL or MOE_ECUDA.
+int enqueue_route_pack_fp8(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_xq,
+                           float* expert_scales, int64_t expert_rows, cudaStream_t s) {
+  const moe_config& c = ctx->cfg;
+  moe::RoutePackFp8Params rp = {};
+  rp.topk_idx = topk_idx;
+  rp.x = static_cast<const uint8_t*>(x);
+  rp.expert_xq = static_cast<uint8_t*>(expert_xq);
+  rp.expert_scales = expert_scales;
+  rp.T = c.num_tokens;
+  rp.K = c.top_k;
+  rp.E = c.num_experts;
+  rp.N = c.num_ranks;
+  rp.H = c.hidden;
+  rp.dst_rows = expert_rows;
+  rp.expert_counts = ctx->expert_counts;
+  rp.expert_offsets = ctx->expert_offsets;
+  rp.src_offsets = ctx->src_offsets;
+  rp.rank_offsets = ctx->rank_offsets;
+  rp.slot_row = ctx->slot_row;
+  rp.row_src = ctx->row_src;
+  rp.error_word = ctx->error_word;
+  rp.queue = ctx->queue;
+
+  const int max_groups = moe::kRoutePackThreads / moe::kRoutePackFp8GroupThreads;
+  auto smem_of = [&](int g, int st) { return moe::route_pack_fp8_smem_bytes(rp.T, rp.K, rp.E, rp.H, g, st); };
+  const size_t optin = static_cast<size_t>(ctx->max_smem_optin);
+  auto stages_for = [&](int g) {  // as many as fit, or as asked; 0 if two do not fit
+    int st = ctx->pack_stages > 0 ? ctx->pack_stages : 16;
+    const int maxst = moe::route_pack_fp8_max_stages(g);
+    if (st > maxst) st = maxst;
+    while (st > 2 && smem_of(g, st) > optin) --st;
+    return smem_of(g, st) <= optin ? st : 0;
+  };
+  auto grid_for = [&](int g) {
+    int64_t grid = (static_cast<int64_t>(rp.T) + g - 1) / g;
+    if (grid > grid_sms(ctx)) grid = grid_sms(ctx);
+    return grid < 1 ? static_cast<int64_t>(1) : grid;
+  };
+  int groups = ctx->pack_ctas_per_sm > 0 ? ctx->pack_ctas_per_sm : ((c.num_tokens + 31) / 32 <= 32 ? 2 : 7);
+  if (groups > max_groups) groups = max_groups;
+  while (groups > 1 && stages_for(groups) == 0) --groups;
+  const int stages = stages_for(groups);
+  if (groups < 1 || stages < 1 || smem_of(groups, stages) > optin) return MOE_EINVAL;
+  const int64_t grid = grid_for(groups);
+  if (moe::launch_route_pack_fp8(rp, static_cast<int>(grid), groups, stages, ctx->pdl != 0, s) != cudaSuccess)
+    return MOE_ECUDA;
+  return MOE_OK;
+}
+
 }  // namespace
 
 MOE_API int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_x,
@@ -1008,6 +1092,17 @@ MOE_API int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* to
       return MOE_EINVAL;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c.num_tokens > 0 && dispatch_fp8_uses_route_pack(ctx)) {
+    const bool timed = ctx->kernel_events != 0;
+    if (timed && cudaEventRecord(ctx->ev[0], s) != cudaSuccess) return MOE_ECUDA;
+    const int frc = enqueue_route_pack_fp8(ctx, x, topk_idx, expert_xq, expert_scales, expert_rows, s);
+    if (frc != MOE_OK) return frc;
+    if (timed && cudaEventRecord(ctx->ev[1], s) != cudaSuccess) return MOE_ECUDA;
+    ctx->pack_timed = timed;
+    ctx->dense_cap = 0;
+    ctx->phase = kDispatched;
+    return MOE_OK;
+  }
   const int rrc = enqueue_routing(ctx, topk_idx, s);
   if (rrc != MOE_OK) return rrc;
   if (c.num_tokens > 0) {

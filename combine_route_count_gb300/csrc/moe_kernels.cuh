@@ -132,6 +132,31 @@ bool route_pack_eligible(int T, int K, int E);
 cudaError_t prepare_route_pack(int max_smem_bytes);  // one-time per-device attribute setup
 cudaError_t launch_route_pack(const RoutePackParams& p, const RoutePackLaunch& l, cudaStream_t stream);
 
+// ---- route_pack_fp8: routing and the fp8 pack in one kernel (small layers) ----
+struct RoutePackFp8Params {
+  const int32_t* topk_idx;  // [T, K]
+  const uint8_t* x;         // bf16 [T, H]
+  uint8_t* expert_xq;       // e4m3 [dst_rows, H]
+  float* expert_scales;     // [dst_rows, H/128]
+  int32_t T, K, E, N, H;    // H % 128 == 0
+  int64_t dst_rows;         // rows of expert_xq / expert_scales (checked builds)
+  int32_t* expert_counts;   // [E]
+  int32_t* expert_offsets;  // [E+1]
+  int32_t* src_offsets;     // [E*N]
+  int32_t* rank_offsets;    // [N+1]
+  int32_t* slot_row;        // [T*K]
+  int32_t* row_src;         // [T*K]
+  int32_t* error_word;      // [1]
+  unsigned long long* queue;  // [2] set to 0 here (may be null)
+};
+constexpr int kRoutePackFp8GroupThreads = 128;  // threads quantising one row together
+size_t route_pack_fp8_smem_bytes(int T, int K, int E, int H, int groups, int stages);
+int route_pack_fp8_max_stages(int groups);
+cudaError_t prepare_route_pack_fp8(int max_smem_bytes);
+// grid CTAs of groups * 128 threads (groups 1..8), `stages` whole-row stages per group.
+cudaError_t launch_route_pack_fp8(const RoutePackFp8Params& p, int grid, int groups, int stages, bool pdl,
+                                  cudaStream_t stream);
+
 struct PackParams {
   const uint8_t* x;         // [T, row_bytes]
   uint8_t* expert_x;        // [rows, row_bytes]

@@ -15,7 +15,8 @@
 // is small for these layers) while its first token rows are already in
 // flight, then its first P warps copy units, each warp with its own ring of
 // shared-memory stages (P "virtual" pack CTAs per SM, as the two-kernel path
-// runs P pack CTAs per SM; one routing per SM instead of P):
+// runs P pack CTAs per SM; one routing per SM instead of P).  Steps 1-4 are
+// the per-CTA routing of route_tables.cuh, shared with route_pack_fp8:
 //
 //   0. one bulk copy (TMA) brings all of topk_idx into shared memory; it is
 //      issued before the token rows so that it does not queue behind them;
@@ -55,6 +56,7 @@
 
 #include "moe_kernels.cuh"
 #include "ptx.cuh"
+#include "route_tables.cuh"
 
 namespace moe {
 namespace {
@@ -62,22 +64,9 @@ namespace {
 constexpr int kMaxStages = 16;
 constexpr int kBarBytes = 512;  // mbarriers: copy warps' stages (<= 63), then the index copy's
 constexpr int kIdxBar = kBarBytes / 8 - 1;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const unsigned long long start = globaltimer();
-  while (!ptx::mbar_try_wait(bar, parity)) {
-    if (globaltimer() - start > kWaitLimitNs) return false;
-  }
-  return true;
-}
+using rtab::index_bytes;
+using rtab::tables_bytes;
+using rtab::wait_phase;
 
 __device__ __forceinline__ void wait_reads_at_most(int depth) {
   switch (depth) {
@@ -92,51 +81,6 @@ __device__ __forceinline__ void wait_reads_at_most(int depth) {
   }
 }
 
-__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
-}
-
-// 32x32 bit-matrix transpose across a warp: bit j of the result in lane i
-// is bit i of the argument in lane j.  Five butterfly stages; stage s swaps,
-// between lanes i and i^s, the bits j whose bit s differs from bit s of i.
-__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
-  constexpr uint32_t lo[5] = {0x0000ffffu, 0x00ff00ffu, 0x0f0f0f0fu, 0x33333333u, 0x55555555u};
-#pragma unroll
-  for (int i = 0; i < 5; ++i) {
-    const int sh = 16 >> i;
-    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, sh);
-    x = (lane & sh) ? ((x & ~lo[i]) | ((y & ~lo[i]) >> sh)) : ((x & lo[i]) | ((y & lo[i]) << sh));
-  }
-  return x;
-}
-
-// Words are scanned in chunks of 32 (one warp scan each): the first row of
-// word q's tokens of expert e is cpre[e][q/32] (the expert's offset plus its
-// rows in earlier chunks) + pre[e][q] (earlier words of its chunk).
-struct Tables {
-  uint32_t* mask;  // [E*NW] tokens of word q that chose expert e, at e*NW+q
-  int32_t* pre;    // [E*NW] #{t in [32*32*(q/32), 32q) : e in idx[t]}
-  int32_t* cpre;   // [E*NC] first row of expert e's tokens in chunk c, at e*NC+c
-  int32_t* off;    // [E+1] expert offsets
-};
-
-__host__ __device__ inline size_t tables_bytes(int T, int E) {
-  const size_t NW = (static_cast<size_t>(T) + 31) / 32;
-  const size_t NC = (NW + 31) / 32;
-  const size_t b =
-      sizeof(int32_t) * (2 * static_cast<size_t>(E) * NW + static_cast<size_t>(E) * NC + static_cast<size_t>(E) + 1);
-  return (b + 15) / 16 * 16;  // the index copy that follows starts 16-byte aligned
-}
-
-__host__ __device__ inline size_t index_bytes(int T, int K) {
-  return (static_cast<size_t>(T) * K * sizeof(int32_t) + 15) / 16 * 16;
-}
-
 // VEC (small rows, at most kVecUnits units of at most kVecChunks*512 bytes
 // per copy warp): the copy warps hold their rows in registers, loaded with
 // 16-byte loads while the tables are built, and store them with 16-byte
@@ -148,19 +92,14 @@ template <int KMAX, bool VEC>
 __global__ void __launch_bounds__(kRoutePackThreads, 1)
     route_pack_kernel(RoutePackParams p, int copy_warps, int stages, int hints, int depth) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int T = p.T, K = p.K, E = p.E, N = p.N;
-  const int NW = (T + 31) / 32;
-  const int NC = (NW + 31) / 32;
+  const int T = p.T, K = p.K, E = p.E;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, W = blockDim.x >> 5;
   const bool copier = warp < copy_warps;
   // This warp's stage ring and mbarriers (copy warps only).
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + (copier ? warp * stages : 0);
   uint8_t* stage_buf = smem + kBarBytes + (copier ? static_cast<size_t>(warp) * stages * p.piece_bytes : 0);
-  Tables tb;
-  tb.mask = reinterpret_cast<uint32_t*>(smem + kBarBytes + static_cast<size_t>(copy_warps) * stages * p.piece_bytes);
-  tb.pre = reinterpret_cast<int32_t*>(tb.mask + static_cast<size_t>(E) * NW);
-  tb.cpre = tb.pre + static_cast<size_t>(E) * NW;
-  tb.off = tb.cpre + static_cast<size_t>(E) * NC;
+  const rtab::Tables tb =
+      rtab::carve_tables(smem + kBarBytes + static_cast<size_t>(copy_warps) * stages * p.piece_bytes, T, E);
   // topk_idx, copied whole: the choices of token t at sidx[t*K .. t*K+K).
   int32_t* sidx = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(tb.mask) + tables_bytes(T, E));
   uint64_t* idx_bar = reinterpret_cast<uint64_t*>(smem) + kIdxBar;
@@ -188,18 +127,7 @@ __global__ void __launch_bounds__(kRoutePackThreads, 1)
   // 0. the indices: one bulk copy of their 16-byte-aligned prefix, issued by
   // the thread that set up its barrier before any token row is requested (so
   // that it does not queue behind the rows), plain loads for the rest.
-  if (tid == 32 * (W - 1)) {
-    ptx::mbar_arrive_expect_tx(idx_bar, static_cast<uint32_t>(bulk_ints) * 4u);
-    if (bulk_ints > 0) ptx::bulk_g2s(sidx, p.topk_idx, static_cast<uint32_t>(bulk_ints) * 4u, idx_bar);
-  }
-  if (blockIdx.x == 0 && tid == 0) {
-    *p.error_word = MOE_OK;  // routing problems are added below; timeouts with atomicCAS
-    if (p.queue) {
-      p.queue[0] = 0ull;  // the pack's unit queue (unused here)
-      p.queue[1] = 0ull;  // the combine's token queue
-    }
-  }
-  for (int i = bulk_ints + tid; i < pairs; i += blockDim.x) sidx[i] = __ldg(p.topk_idx + i);
+  rtab::start_index_copy(p, sidx, idx_bar, bulk_ints, 32 * (W - 1));
   __syncthreads();
 
   auto piece_bytes = [&](int j) -> uint32_t {
@@ -261,123 +189,11 @@ __global__ void __launch_bounds__(kRoutePackThreads, 1)
     return;
   }
 
-  // 1. per-(expert, word) token masks; index checks.
-  bool bad = false;
-  for (int q = warp; q < NW; q += W) {
-    const int t = q * 32 + lane;
-    int e[KMAX];
-#pragma unroll
-    for (int k = 0; k < KMAX; ++k) e[k] = (k < K && t < T) ? sidx[t * K + k] : -1;
-    if (t < T) {
-#pragma unroll
-      for (int k = 0; k < KMAX; ++k) {
-        if (k < K) {
-          if (static_cast<unsigned>(e[k]) >= static_cast<unsigned>(E)) {
-            bad = true;
-            e[k] = -1;
-          } else {
-#pragma unroll
-            for (int j = 0; j < k; ++j) bad |= (e[j] == e[k]);
-          }
-        }
-      }
-    }
-    // Per group of 32 experts: lane t sets bit x for each expert 32g+x it
-    // chose; transposing that 32x32 bit matrix across the warp leaves in lane
-    // x the word's mask of expert 32g+x.
-    for (int g0 = 0; g0 < E; g0 += 32) {
-      uint32_t bits = 0u;
-#pragma unroll
-      for (int k = 0; k < KMAX; ++k)
-        if (k < K && e[k] >= g0 && e[k] < g0 + 32) bits |= 1u << (e[k] - g0);
-      bits = warp_transpose32(bits, lane);
-      if (g0 + lane < E) tb.mask[(g0 + lane) * NW + q] = bits;
-    }
-  }
-  bad = __syncthreads_or(bad);
-
-  // 2. per (expert, chunk of 32 words): exclusive prefix of the word
-  // popcounts inside the chunk, and the chunk's total.
-  for (int pc = warp; pc < E * NC; pc += W) {
-    const int ex = pc / NC;
-    const int q = (pc - ex * NC) * 32 + lane;
-    const int c = q < NW ? __popc(tb.mask[ex * NW + q]) : 0;
-    const int incl = warp_incl_scan(c, lane);
-    if (q < NW) tb.pre[ex * NW + q] = incl - c;
-    if (lane == 31) tb.cpre[pc] = incl;
-  }
-  __syncthreads();
-  // 3. one exclusive scan over the chunk totals in (expert, chunk) order
-  // gives both: cpre[e][c] becomes the first row of expert e's tokens in
-  // chunk c, so cpre[e][0] is the expert's offset.  One warp, each lane a
-  // run of consecutive totals.
-  if (warp == 0) {
-    const int L = E * NC;
-    const int m = (L + 31) / 32;
-    const int lo = min(L, lane * m), hi = min(L, lo + m);
-    int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += tb.cpre[i];
-    const int incl = warp_incl_scan(sum, lane);
-    int run = incl - sum;
-    for (int i = lo; i < hi; ++i) {
-      const int v = tb.cpre[i];
-      tb.cpre[i] = run;
-      run += v;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    __syncwarp();
-    for (int ex = lane; ex < E; ex += 32) tb.off[ex] = tb.cpre[ex * NC];
-    if (lane == 0) tb.off[E] = total;
-  }
-  __syncthreads();
-
-  // Stable row of token t's choice of expert e (t < T).
-  auto row_of = [&](int t, int e) -> int {
-    const int q = t >> 5;
-    return tb.cpre[e * NC + (q >> 5)] + tb.pre[e * NW + q] + __popc(tb.mask[e * NW + q] & ((1u << (t & 31)) - 1u));
-  };
-
-  // 4. this CTA's tokens b, b+G, ...: slot_row and row_src.
-  const int G = gridDim.x;
-  const int my_tokens = T > static_cast<int>(blockIdx.x) ? (T - static_cast<int>(blockIdx.x) + G - 1) / G : 0;
-  for (int i = tid; i < my_tokens * K; i += blockDim.x) {
-    const int t = static_cast<int>(blockIdx.x) + (i / K) * G;
-    const int k = i - (i / K) * K;
-    const int64_t pair = static_cast<int64_t>(t) * K + k;
-    if (bad) {
-      p.slot_row[pair] = -1;
-    } else {
-      const int r = row_of(t, sidx[pair]);
-      p.slot_row[pair] = r;
-      p.row_src[r] = static_cast<int32_t>(pair);
-    }
-  }
-  if (blockIdx.x == 0) {
-    if (bad) {
-      for (int i = tid; i < E; i += blockDim.x) p.expert_counts[i] = 0;
-      for (int i = tid; i <= E; i += blockDim.x) p.expert_offsets[i] = 0;
-      for (int i = tid; i <= N; i += blockDim.x) p.rank_offsets[i] = 0;
-      for (int i = tid; i < E * N; i += blockDim.x) p.src_offsets[i] = 0;
-      if (tid == 0) atomicExch(p.error_word, MOE_EROUTE);
-    } else {
-      const int Tr = T / N, L = E / N;
-      for (int i = tid; i < E; i += blockDim.x) p.expert_counts[i] = tb.off[i + 1] - tb.off[i];
-      for (int i = tid; i <= E; i += blockDim.x) p.expert_offsets[i] = tb.off[i];
-      for (int r = tid; r <= N; r += blockDim.x) p.rank_offsets[r] = r < N ? tb.off[r * L] : tb.off[E];
-      // First row of (expert e, source rank s): the rows of e that tokens
-      // before s*T/N took.
-      for (int i = tid; i < E * N; i += blockDim.x) {
-        const int ex = i / N, s = i - (i / N) * N;
-        p.src_offsets[i] = row_of(s * Tr, ex);
-      }
-      // Receive bound of one rank: N * (T/N) * max(K, E/N) rows.
-      const int64_t bound = static_cast<int64_t>(N) * Tr * (K > L ? K : L);
-      bool over = false;
-      for (int r = tid; r < N; r += blockDim.x) over |= (tb.off[(r + 1) * L] - tb.off[r * L]) > bound;
-      over = __syncthreads_or(over);
-      if (tid == 0 && over) atomicCAS(p.error_word, MOE_OK, MOE_EBOUND);
-    }
-  }
+  // 1.-4. the routing tables, the CTA's slot_row / row_src entries and (CTA 0)
+  // the counts, offsets and status.
+  const bool bad = __syncthreads_or(rtab::token_masks<KMAX>(sidx, tb, T, K, E));
+  rtab::expert_scans(tb, E);
+  rtab::write_routing(p, tb, sidx, bad);
   if (!copier) return;
 
   if (bad) {
@@ -394,7 +210,7 @@ __global__ void __launch_bounds__(kRoutePackThreads, 1)
     for (int u = 0; u < (VEC ? kVecUnits : 1); ++u) {
       if (u < mine) {
         const int t = static_cast<int>(first + u * step);
-        const int my_row = lane < K ? row_of(t, sidx[t * K + lane]) : -1;
+        const int my_row = lane < K ? rtab::row_of(tb, t, sidx[t * K + lane]) : -1;
         for (int k = 0; k < K; ++k) {
           const int row = __shfl_sync(0xffffffffu, my_row, k);
           if (kChecked && row >= p.dst_rows) {
@@ -417,7 +233,7 @@ __global__ void __launch_bounds__(kRoutePackThreads, 1)
   // unit ahead.
   auto dest_row = [&](int64_t unit_index) -> int {
     const int tt = static_cast<int>((first + unit_index * step) / p.pieces);
-    return lane < K ? row_of(tt, sidx[tt * K + lane]) : -1;
+    return lane < K ? rtab::row_of(tb, tt, sidx[tt * K + lane]) : -1;
   };
   int64_t i = 0;
   bool ok = true;

@@ -37,6 +37,7 @@ MOE_OPT_FP8_ORDER = 18
 MOE_OPT_KERNEL_EVENTS = 19
 MOE_OPT_PACK_SCHEDULE = 20
 MOE_OPT_COMBINE_SCHEDULE = 21
+MOE_OPT_ROUTE_VARIANT_FP8 = 22  # read only: the routing moe_dispatch_send_fp8 takes
 PACK_BULK, PACK_VECTOR = 0, 1
 
 # Every entry point of include/moe.h.

@@ -149,9 +149,12 @@ int moe_dispatch_send(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void
  *   expert_xq      device E4M3 bytes [expert_rows, H], 16-byte aligned
  *   expert_scales  device float32 [expert_rows, H / MOE_FP8_BLOCK]
  *   expert_rows    >= T*K; rows [0, T*K) of both are written
- * The combine that follows still takes bf16 expert outputs.  Valid in the
- * idle phase; MOE_EINVAL if H is not a multiple of the block or a bf16 row
- * is too large for two shared-memory stages. */
+ * The combine that follows still takes bf16 expert outputs.  For the small
+ * layers of moe_dispatch_send's route_pack, routing and quantisation run as
+ * one kernel, route_pack_fp8 (MOE_OPT_ROUTE_VARIANT_FP8 reports the path);
+ * the results are the same either way.  Valid in the idle phase; MOE_EINVAL
+ * if H is not a multiple of the block or a bf16 row is too large for two
+ * shared-memory stages. */
 #define MOE_FP8_BLOCK 128
 int moe_dispatch_send_fp8(moe_ctx* ctx, const void* x, const int32_t* topk_idx, void* expert_xq,
                           float* expert_scales, int64_t expert_rows, void* stream);
@@ -302,12 +305,17 @@ int moe_partial_rows(const moe_config* cfg, int64_t* rows);
  *                             always uses the vector copy)
  *   MOE_OPT_PACK_STAGES       shared-memory stages per bulk CTA, 2..16, 0 =
  *                             automatic (about 200 KiB of stages per SM, default;
- *                             fp8 pack: about 72 KiB per CTA for K >= 4, else 3)
+ *                             fp8 pack: about 72 KiB per CTA for K >= 4, else 3;
+ *                             route_pack_fp8: whole-row stages per group of 128
+ *                             threads, as many as fit)
  *   MOE_OPT_PACK_PIECE_BYTES  bytes of a row moved per work unit, a multiple of
  *                             16, 0 = automatic (whole row up to 8 KiB, else
  *                             equal pieces of at most 8 KiB)
  *   MOE_OPT_PACK_CTAS_PER_SM  0 = automatic (bulk variant: 2 for K >= 4, else 3;
- *                             fp8 pack: 3 for K >= 4, else up to 8), else 1..32
+ *                             fp8 pack: 3 for K >= 4, else up to 8;
+ *                             route_pack: copy warps per CTA; route_pack_fp8:
+ *                             groups of 128 threads per CTA, at most 8), else
+ *                             1..32
  *   MOE_OPT_PDL               1 = launch pack/combine with programmatic
  *                             dependent launch (default), 0 = plain launches
  *   MOE_OPT_ROUTE_VARIANT     routing kernels: 0 = automatic (for
@@ -323,8 +331,12 @@ int moe_partial_rows(const moe_config* cfg, int64_t* rows);
  *                             in one kernel, every CTA of the pack grid
  *                             computing the routing tables itself (bulk
  *                             copies, static split; MOE_EINVAL unless
- *                             T*K <= 16384 and E*ceil(T/32) <= 4096; the
- *                             other dispatch calls route as with 0) */
+ *                             T*K <= 16384 and E*ceil(T/32) <= 4096), and
+ *                             moe_dispatch_send_fp8 routes and quantises in
+ *                             one kernel, route_pack_fp8 (automatic too for
+ *                             those layers with MOE_OPT_FP8_ORDER 1 and no
+ *                             forced pack queue); the other dispatch calls
+ *                             route as with 0 */
 #define MOE_OPT_PACK_VARIANT 1
 #define MOE_OPT_PACK_STAGES 2
 #define MOE_OPT_PACK_PIECE_BYTES 3
@@ -336,8 +348,11 @@ int moe_ctx_set_option(moe_ctx* ctx, int option, int64_t value);
 /* Reads back a launch option.  For MOE_OPT_ROUTE_VARIANT set to 0
  * (automatic) it reports the path moe_dispatch_send will take (2, 3 or 4);
  * MOE_OPT_ROUTE_CLUSTER_CTAS reports the route_cluster cluster size chosen
- * for this configuration (0 if the device cannot schedule it). */
+ * for this configuration (0 if the device cannot schedule it);
+ * MOE_OPT_ROUTE_VARIANT_FP8 (read only) the routing of
+ * moe_dispatch_send_fp8 in the same numbering (4: route_pack_fp8). */
 #define MOE_OPT_ROUTE_CLUSTER_CTAS 7
+#define MOE_OPT_ROUTE_VARIANT_FP8 22
 /*   MOE_OPT_COMBINE_VARIANT     0 = a producer warp gathers the K expert-row
  *                               pieces with bulk copies into shared-memory
  *                               stages, consumer warps reduce; 1 = one thread

@@ -6,7 +6,8 @@ bit-exact against the oracle (the checks never fire on valid tables); then one
 slot_row entry in the workspace is overwritten with T*K, one row past the
 expert outputs handed to combine_send, and each combine form must report
 MOE_ECORRUPT, write nothing for that token and still write every other token
-bit-exact.  The expert-output buffer has guard rows after it, so the entry
+bit-exact.  The fp8 dispatch runs clean and bit-exact in the checked build
+too.  The expert-output buffer has guard rows after it, so the entry
 points inside the allocation even if a check were missing."""
 import json
 import os
@@ -74,6 +75,22 @@ for name, opts in (("bulk", dict(combine_variant=0)), ("vector", dict(combine_va
     res[name] = dict(clean=bool(clean), status=int(status), token_untouched=bool(np.all(o[5] == SENT)),
                      others_exact=bool(np.array_equal(o[others], want[others])))
     layer.close()
+# fp8 dispatch in the checked build, both forms (routing inside the fp8 pack,
+# and route_cluster + the fp8 pack): bit-exact, no check fires.
+_, xq_ref, xs_ref = oracle.dispatch_fp8(li.x, li.topk_idx, w.E, w.N)
+for name, route in (("fp8_fused", 4), ("fp8_two_kernel", 3)):
+    layer = moe.MoELayer(T, H, K, w.E, w.N, route_variant=route)
+    xq = torch.zeros((rows, H), dtype=torch.uint8, device="cuda")
+    xs = torch.zeros((rows, H // 128), dtype=torch.float32, device="cuda")
+    layer.dispatch_send_fp8(x, idx, xq, xs)
+    layer.dispatch_recv()
+    layer.combine_send(y)
+    out = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    layer.combine_recv(wt, out)
+    res[name] = dict(status=int(layer.get_error()), codes=bool(np.array_equal(xq.cpu().numpy(), xq_ref)),
+                     scales=bool(np.array_equal(xs.cpu().numpy().view(np.uint32), xs_ref.view(np.uint32))),
+                     out=bool(np.array_equal(out.cpu().numpy().view(np.uint16), ref)))
+    layer.close()
 print(json.dumps(res))
 """
 
@@ -86,6 +103,9 @@ def test_checked_build_detects_a_corrupt_table_entry():
                        timeout=900, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-3000:]
     res = json.loads(r.stdout.strip().splitlines()[-1])
+    for name in ("fp8_fused", "fp8_two_kernel"):
+        v = res.pop(name)
+        assert v == dict(status=moe.MOE_OK, codes=True, scales=True, out=True), (name, v)
     for name, v in res.items():
         assert v["clean"], (name, v)
         assert v["status"] == moe.MOE_ECORRUPT, (name, v)
