@@ -807,15 +807,18 @@ def run_e2e(args, w, li, layer, stream, dev):
     run(4)
     torch.cuda.synchronize(dev)
     # The host link on this machine, measured alone with the same copies: the
-    # floor the end-to-end step cannot beat (uploads dominate it).
-    l0 = torch.cuda.Event(enable_timing=True)
-    l1 = torch.cuda.Event(enable_timing=True)
-    l0.record(s_up)
-    for _ in range(4):
-        upload(0)
-    l1.record(s_up)
-    torch.cuda.synchronize(dev)
-    h2d_gbs = 4 * h2d / (l0.elapsed_time(l1) * 1e-3) / 1e9
+    # floor the end-to-end step cannot beat (uploads dominate it).  Best of
+    # three runs of four uploads (one run has read a third of the link's rate).
+    h2d_gbs = 0.0
+    for _ in range(3):
+        l0 = torch.cuda.Event(enable_timing=True)
+        l1 = torch.cuda.Event(enable_timing=True)
+        l0.record(s_up)
+        for _ in range(4):
+            upload(0)
+        l1.record(s_up)
+        torch.cuda.synchronize(dev)
+        h2d_gbs = max(h2d_gbs, 4 * h2d / (l0.elapsed_time(l1) * 1e-3) / 1e9)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(s_up)
