@@ -569,3 +569,55 @@ def test_route_pack_resets_the_combine_queue_every_layer(moe, oracle_mod):
         assert np.array_equal(lay["slot_row"].cpu().numpy(), d.slot_row)
         assert np.array_equal(ex.cpu().numpy().view(np.uint16), d.expert_x), n
         assert np.array_equal(out.cpu().numpy().view(np.uint16), out_ref), n
+
+
+UNALIGNED_SHAPES = [  # (T, H, K, E, N): T*K not a multiple of 4 for the odd ones
+    (64, 256, 2, 8, 2),
+    (1000, 136, 5, 40, 4),
+    (3, 24, 3, 3, 1),
+    (4096, 512, 8, 256, 32),
+]
+
+
+@pytest.mark.parametrize("route", [0, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("shape", UNALIGNED_SHAPES, ids=["x".join(map(str, s)) for s in UNALIGNED_SHAPES])
+def test_index_array_four_bytes_off_a_16_byte_boundary(moe, oracle_mod, shape, route):
+    """topk_idx that is 4-byte aligned but not 16-byte aligned: the routing
+    kernels then load every index with plain loads instead of bulk or
+    16-byte vector copies; bf16 and fp8 payloads, every routing kernel."""
+    T, H, K, E, N = shape
+    w = gen.custom("unaligned", T=T, H=H, K=K, E=E, N=N, seed_index=131)
+    li = gen.make_inputs(w)
+    layer = moe.MoELayer(T, H, K, E, N)
+    try:
+        layer.set_option(moe.MOE_OPT_ROUTE_VARIANT, route)
+    except moe.MoEError:
+        pytest.skip("route variant not available for this shape")
+    d, out_ref = oracle_of(oracle_mod, w, li)
+    big = torch.zeros(T * K + 4, dtype=torch.int32, device="cuda")
+    big[1:1 + T * K] = _dev(li.topk_idx).view(-1)
+    idx = big[1:1 + T * K].view(T, K)
+    assert idx.data_ptr() % 16 == 4
+    x, wt, y = _dev(li.x.view(np.int16)), _dev(li.topk_w), _dev(li.y.view(np.int16))
+    ex = torch.zeros((T * K, H), dtype=torch.int16, device="cuda")
+    out = torch.zeros((T, H), dtype=torch.int16, device="cuda")
+    lay = layer.layer(x, idx, wt, ex, y, out)
+    assert layer.get_error() == moe.MOE_OK
+    assert np.array_equal(lay["slot_row"].cpu().numpy(), d.slot_row)
+    assert np.array_equal(lay["row_src"].cpu().numpy(), d.row_src)
+    assert np.array_equal(lay["src_offsets"].cpu().numpy().reshape(-1), d.src_offsets.reshape(-1))
+    assert np.array_equal(ex.cpu().numpy().view(np.uint16), d.expert_x)
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), out_ref)
+    if H % 128 == 0:
+        _, xq_ref, xs_ref = oracle_mod.dispatch_fp8(li.x, li.topk_idx, E, N)
+        xq = torch.zeros((T * K, H), dtype=torch.uint8, device="cuda")
+        xs = torch.zeros((T * K, H // 128), dtype=torch.float32, device="cuda")
+        layer.dispatch_send_fp8(x, idx, xq, xs)
+        lay = layer.dispatch_recv()
+        layer.combine_send(y)
+        layer.combine_recv(wt, out)
+        assert layer.get_error() == moe.MOE_OK
+        assert np.array_equal(lay["slot_row"].cpu().numpy(), d.slot_row)
+        assert np.array_equal(xq.cpu().numpy(), xq_ref)
+        assert np.array_equal(xs.cpu().numpy().view(np.uint32), xs_ref.view(np.uint32))
+    layer.close()
