@@ -56,7 +56,7 @@ def parse():
                          "bf16 matmul, random weights) the split send/receive layer hides, per MOE_OPT_MAX_SMS, "
                          "and a two-micro-batch pipeline against the same work in sequence")
     ap.add_argument("--graph", action="store_true",
-                    help="capture one step per buffer set in a CUDA graph and replay it")
+                    help="capture 16 steps (alternating the buffer sets) in a CUDA graph and replay it")
     return ap.parse_args()
 
 
@@ -367,19 +367,21 @@ def run_gpu(args):
 
     run_steps = None
     if args.graph:
-        # One replay = one step on each buffer set, in order.
+        # One replay = GRAPH_LAYERS steps, alternating the buffer sets; the
+        # remainder of K runs as direct calls.
         graph = torch.cuda.CUDAGraph()
+        per_graph = GRAPH_LAYERS - GRAPH_LAYERS % len(sets)
         with torch.cuda.graph(graph, stream=stream):
-            for s_ in sets:
-                step(s_)
+            for i in range(per_graph):
+                step(sets[i % len(sets)])
         torch.cuda.synchronize(dev)
 
         def run_steps(k):
             with torch.cuda.stream(stream):
-                for _ in range(k // len(sets)):
+                for _ in range(k // per_graph):
                     graph.replay()
-            for i in range(k % len(sets)):
-                step(sets[i])
+            for i in range(k % per_graph):
+                step(sets[i % len(sets)])
 
     clocks = ClockSampler(torch.cuda.current_device() if ws == 1 else local).start()
     time.sleep(0.2)
@@ -560,8 +562,10 @@ def run_gpu(args):
             workloads[key] = time_workload(name, payload, max(n, min(args.steps, 4 * n)), dev, peak)
         workloads["clocks"] = wclocks.stop(t_w0, time.time())
         workloads["method"] = ("two rotating buffer sets, one pair of CUDA events around `steps` layers; us: direct "
-                               "C-ABI calls from Python, us_graph: the same calls replayed from a CUDA graph; frac: "
-                               "algorithmic bytes / the faster of the two / measured copy peak")
+                               f"C-ABI calls from Python, us_graph: the same calls, {GRAPH_LAYERS} layers per CUDA "
+                               "graph, replayed; us_graph_2: two layers per graph (each replay adds the graph "
+                               "launch's gap); frac: algorithmic bytes / the faster of us and us_graph / measured "
+                               "copy peak")
 
     cpu = None
     if not args.no_cpu and rank == 0:
@@ -579,7 +583,8 @@ def run_gpu(args):
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": f"inputs > L2: {ab['total'] / 1e6:.0f} MB moved per layer, "
                              f"{args.buffer_sets} rotating buffer sets",
-                       "launch": "CUDA graph replay" if args.graph else "direct C-ABI calls",
+                       "launch": f"CUDA graph replay, {GRAPH_LAYERS} layers per graph" if args.graph
+                                 else "direct C-ABI calls",
                        "payload": args.payload,
                        "dispatch": "direct placement" if args.dispatch == "direct"
                                    else "two-stage: per-peer send rows, then receive shuffle",
@@ -621,6 +626,10 @@ def run_gpu(args):
 # Steps per workload: at least ~20 ms of timed layers.
 EXTRA_WORKLOADS = [("tiny", "bf16", 4000), ("mixtral", "bf16", 1000), ("kimi", "bf16", 60), ("worst", "bf16", 120),
                    ("deepseek", "fp8", 300), ("deepseek", "dense", 10)]
+
+
+# Layers per CUDA graph in the graph-replay timings.
+GRAPH_LAYERS = 16
 
 
 def time_workload(name, payload, steps, dev, peak, warmup=10):
@@ -685,21 +694,30 @@ def time_workload(name, payload, steps, dev, peak, warmup=10):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     us = e0.elapsed_time(e1) / steps * 1e3
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for s_ in sets:
-            step(s_)
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            graph.replay()
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(steps // 2):
-            graph.replay()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    us_graph = e0.elapsed_time(e1) / (2 * (steps // 2)) * 1e3
+    # Graph replay: GRAPH_LAYERS layers (alternating the two buffer sets) per
+    # graph, as a model's graph holds many layers; and one layer per set (two
+    # per graph), where every replay adds the graph launch's own gap.
+    def graph_us(layers):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(layers):
+                step(sets[i % 2])
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        torch.cuda.synchronize(dev)
+        replays = max(1, steps // layers)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(replays):
+                graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        del graph
+        return e0.elapsed_time(e1) / (replays * layers) * 1e3
+
+    us_graph = graph_us(GRAPH_LAYERS)
+    us_graph_2 = graph_us(2)
     status = layer.get_error(stream)
     if status != moe.MOE_OK:
         raise RuntimeError(f"device reported status {status} timing {name}")
@@ -708,11 +726,12 @@ def time_workload(name, payload, steps, dev, peak, warmup=10):
                4: "route_pack (in the pack)" if payload != "fp8" else "route_pack_fp8 (in the fp8 pack)",
                5: "route_pack (one CTA)"}[v]
     layer.close()
-    del sets, graph, blocks
+    del sets, blocks
     torch.cuda.empty_cache()
     ab = algorithmic_bytes(w, "bf16" if payload == "dense" else payload, dense_cap=cap)["total"]
     best = min(us, us_graph)
-    res = {"us": round(us, 2), "us_graph": round(us_graph, 2), "bytes": ab, "steps": steps,
+    res = {"us": round(us, 2), "us_graph": round(us_graph, 2), "us_graph_2": round(us_graph_2, 2), "bytes": ab,
+           "steps": steps,
            "tbs": round(ab / best / 1e6, 3), "frac": round(ab / best / 1e3 / peak, 4),
            "payload": "bf16" if payload == "dense" else payload, "routing": routing}
     if cap is not None:
