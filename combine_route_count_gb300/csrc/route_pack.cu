@@ -48,7 +48,7 @@
 // matters: with per-lane global loads the compiler may issue each word's
 // loads just before their use, and a Mixtral-sized layer spent ~15 us of
 // serialised round trips (queued behind the token rows) in step 1.  Every
-// CTA reaches the same verdict on a malformed routing, so after a routing
+// CTA reaches the same decision on a malformed routing, so after a routing
 // error no CTA copies anything and every slot_row entry becomes -1 (the
 // combine then writes nothing).
 

@@ -24,7 +24,7 @@
 //   rows from the tables in shared memory), a barrier of the group, refill
 //   the stage with the group's token `stages` further on.
 //
-// After a routing error every CTA reaches the same verdict: nothing is
+// After a routing error every CTA reaches the same decision: nothing is
 // written but slot_row = -1 and the zeroed tables.  Waits are bounded (2 s)
 // and report MOE_ETIMEDOUT; a group that gives up waits (bounded) for its
 // loads in flight before it exits.

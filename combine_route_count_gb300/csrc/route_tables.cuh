@@ -22,7 +22,7 @@
 //      CTA 0 also the counts, offsets, per-(expert, source rank) and per-rank
 //      offsets and the status word.
 //
-// Every CTA computes the same tables and reaches the same verdict on a
+// Every CTA computes the same tables and reaches the same decision on a
 // malformed routing.
 
 #pragma once
@@ -228,7 +228,7 @@ __device__ __forceinline__ int row_of(const Tables& tb, int t, int e) {
 
 // Step 4, all threads of the CTA: slot_row and row_src of tokens b, b+G, ...
 // (every slot_row entry -1 after a routing error); CTA 0 writes the counts,
-// offsets and status.  `bad` is the CTA-wide verdict.
+// offsets and status.  `bad` is the CTA-wide decision.
 template <class P>
 __device__ __forceinline__ void write_routing(const P& p, const Tables& tb, const int32_t* sidx, bool bad) {
   const int T = p.T, K = p.K, E = p.E, N = p.N;
