@@ -108,7 +108,9 @@ def measured_peaks():
 
 def committed_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or
-    None when the kernel source changed since it was captured."""
+    None when the kernel source changed since it was captured: the record's
+    source_sha covers its .cu file and the headers that hold only that
+    kernel's device code (kernel_headers)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -118,12 +120,13 @@ def committed_traffic(kernel: str, workload: str):
     entry = rec.get(workload, {}).get(kernel)
     if not entry:
         return None
-    src = os.path.join(ROOT, "combine_route_count_gb300", "csrc", entry["source"])
+    h = hashlib.sha256()
     try:
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for name in [entry["source"]] + entry.get("kernel_headers", []):
+            h.update(open(os.path.join(ROOT, "combine_route_count_gb300", "csrc", name), "rb").read())
     except OSError:
         return None
-    return entry["dram_bytes_per_launch"] if sha == entry["source_sha"] else None
+    return entry["dram_bytes_per_launch"] if h.hexdigest()[:16] == entry["source_sha"] else None
 
 
 class ClockSampler:
