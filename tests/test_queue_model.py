@@ -14,6 +14,10 @@ against one shared counter, and check the protocol's invariants:
     loaded one unit ahead always belong to the CTA's next unit;
   - claims stop at the first value past the end, so the counter grows by at
     most the claimed work plus a few claims per CTA.
+
+The per-group stage ring of route_pack_fp8 (csrc/route_pack_fp8.cu) is
+modelled the same way, with mbarrier phases as counts: every wait is
+satisfied by the phase of its own token's load, never an older one.
 """
 import random
 
@@ -186,3 +190,49 @@ def test_fp8_token_queue(T, G, stages):
         seen = []
         _run([_fp8_cta(b, G, T, stages, counter, seen) for b in range(G)], seed)
         assert sorted(seen) == list(range(T))
+
+
+def _fused_fp8_group(stages, mine, rng, seen):
+    """route_pack_fp8, one group of 128 threads: its first thread loads tokens
+    0..stages-1 of the group into its own ring before the routing; per token
+    i the group waits on stage i % stages with parity (i / stages) & 1,
+    quantises, synchronises, and refills the stage with token i + stages.
+    Loads land after random delays; the mbarrier of a stage is modelled by
+    its count of completed phases (try_wait with parity P succeeds once the
+    count's parity differs from P)."""
+    completed = [0] * stages           # phases completed per stage
+    in_flight = []                     # (stage, token) loads not landed yet
+    content = [None] * stages          # token whose row a landed load left in the stage
+    for i in range(min(stages, mine)):
+        in_flight.append((i % stages, i))
+
+    def land_some():
+        rng.shuffle(in_flight)
+        for _ in range(rng.randint(0, len(in_flight))):
+            s, t = in_flight.pop()
+            content[s] = t
+            completed[s] += 1
+
+    for i in range(mine):
+        s, parity = i % stages, (i // stages) & 1
+        while (completed[s] & 1) == parity:  # try_wait.parity fails: not landed yet
+            land_some()
+            yield
+        # The phase that satisfied the wait is this token's load, not an older one.
+        assert completed[s] == i // stages + 1
+        assert content[s] == i
+        seen.append(i)
+        if i + stages < mine:
+            assert all(st != s for st, _ in in_flight), "a stage is refilled only once it is free"
+            in_flight.append((s, i + stages))
+        yield
+    assert not in_flight
+
+
+@pytest.mark.parametrize("stages,mine", [(1, 5), (2, 2), (2, 7), (3, 4), (3, 3), (7, 30), (16, 40), (4, 0)])
+def test_fused_fp8_stage_ring(stages, mine):
+    for seed in range(300):
+        rng = random.Random(seed)
+        seen = []
+        _run([_fused_fp8_group(stages, mine, rng, seen)], seed)
+        assert seen == list(range(mine))
