@@ -239,7 +239,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "workload"},
-                   "parallelism": "replicas"},
+                   "parallelism": "replicas" if ws > 1 else "single"},
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
