@@ -116,6 +116,7 @@ FUSED_SHAPES = [  # (T, H, K, E, N, router): route_pack_fp8 (T*K <= 16384, E*cei
     (257, 384, 2, 8, 1, "uniform_random"),  # ragged: not a multiple of the groups
     (1, 128, 1, 1, 1, "uniform_random"),
     (96, 2304, 3, 12, 3, "uniform_random"),  # odd K, 18 blocks
+    (256, 16384, 2, 8, 2, "uniform_random"),  # 32 KiB rows: few stages fit
 ]
 FUSED_OPTIONS = [
     dict(),
