@@ -183,6 +183,36 @@ __device__ __forceinline__ bool token_masks(const int32_t* sidx, const Tables& t
 __device__ __forceinline__ void expert_scans(const Tables& tb, int E) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
   const int NW = tb.NW, NC = tb.NC;
+  if (E * NC <= 32 && NW <= 8) {
+    // Few experts and words (up to 256 tokens): one warp, lane pc walks the
+    // words of its chunk (word prefixes and the chunk total), then one warp
+    // scan over the chunk totals in (expert, chunk) order; one CTA barrier
+    // instead of two.  Measured on GB300 (A/B, 20-layer graphs): 64-token
+    // layer 4.82 -> 4.61 us, its fp8 form 5.64 -> 5.43 us.  With 32 words per
+    // chunk the serial walk is slower than the two scans (Mixtral-sized layer
+    // 34.15 -> 36.6 us).
+    if (warp == 0) {
+      const int L = E * NC;
+      int total = 0;
+      if (lane < L) {
+        const int ex = lane / NC;
+        const int q0 = (lane - ex * NC) * 32;
+        const int q1 = q0 + 32 < NW ? q0 + 32 : NW;
+        for (int q = q0; q < q1; ++q) {
+          tb.pre[ex * NW + q] = total;
+          total += __popc(tb.mask[ex * NW + q]);
+        }
+      }
+      const int incl = warp_incl_scan(total, lane);
+      if (lane < L) tb.cpre[lane] = incl - total;
+      const int all = __shfl_sync(0xffffffffu, incl, 31);
+      __syncwarp();
+      for (int ex = lane; ex < E; ex += 32) tb.off[ex] = tb.cpre[ex * NC];
+      if (lane == 0) tb.off[E] = all;
+    }
+    __syncthreads();
+    return;
+  }
   // Per (expert, chunk of 32 words): exclusive prefix of the word popcounts
   // inside the chunk, and the chunk's total.
   for (int pc = warp; pc < E * NC; pc += W) {
