@@ -1217,6 +1217,7 @@ int enqueue_combine(moe_ctx* ctx, const void* y, int64_t y_rows, const int32_t* 
   cl.pdl = ctx->pdl != 0;
   cl.variant = combine_variant_of(ctx);
   cl.grid = 0;
+  cl.sms = grid_sms(ctx);
   if (cl.variant == moe::kCombineBulk) {
     // By default the CTAs take tokens in the strided order (the leftover
     // tokens split evenly by pieces) with pieces of up to 4 KiB; measured on

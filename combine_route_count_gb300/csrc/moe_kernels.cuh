@@ -233,6 +233,7 @@ struct CombineLaunch {
   int grid;                // bulk: CTAs
   BulkCombineShape shape;  // bulk
   bool pdl;                // launch with programmatic stream serialization
+  int sms;                 // vector: SMs the grid may spread over
 };
 size_t combine_bulk_smem_bytes(const BulkCombineShape& sh, int K);
 // Stages and pieces of the bulk combine; piece_bytes <= 0 picks equal pieces
